@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Benchmark of the K-quant matvec on GB300: achieved HBM GB/s and us/call.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--ntok T]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+by default the Muse Glimmer QKV+gate concurrent set at ntok=1 (Q and gate
+4096x6656 Q4_K, K and V 256x6656 Q6_K, one shared x) in ONE kq_matvec_set
+launch.  Other workloads (--workload) time the single-matrix shapes, the
+Q6_K+Q5_K grid-split pair and the LM head.
+
+Timing (ours): inputs resident in HBM; K steps replayed from CUDA graphs,
+bracketed by CUDA events on the launching stream with a barrier and a device
+synchronize on both sides; the weights rotate over enough copies that their
+total exceeds three times the L2 size, so every step streams from HBM.
+`value` = algorithmic bytes (weights + x once per distinct plane + y) of all
+steps on all ranks / max-over-ranks elapsed time.  `e2e` times the public
+Python API with the per-step input x copied from pinned host memory and the
+outputs copied back inside the timed region (weights stay resident, as model
+weights do).  `cpu_baseline` times the CPU oracle on a bounded sample.
+
+--impl reference times the CPU oracle itself (single thread) on a bounded
+sample of the same workload each step, and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from quant_quantized_matvec_gb300 import synth  # noqa: E402
+
+Q4_K, Q5_K, Q6_K = synth.Q4_K, synth.Q5_K, synth.Q6_K
+METRIC = ("achieved HBM GB/s (% of GB300 peak) and us per K-quant matvec, "
+          "ntok=1")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- workloads
+def workload(name: str, ntok: int):
+    """-> (members [(fmt, rows, cols, x_plane)], description)."""
+    if name == "qkv_gate_set":
+        return ([(Q4_K, 4096, 6656, 0), (Q6_K, 256, 6656, 0),
+                 (Q6_K, 256, 6656, 0), (Q4_K, 4096, 6656, 0)],
+                "Muse Glimmer QKV+gate concurrent set: Q,gate 4096x6656 Q4_K;"
+                " K,V 256x6656 Q6_K; shared x; one kq_matvec_set launch")
+    if name in ("q4k_4096", "q5k_4096", "q6k_4096"):
+        fmt = {"q4k": Q4_K, "q5k": Q5_K, "q6k": Q6_K}[name[:3]]
+        return ([(fmt, 4096, 6656, 0)],
+                f"single {synth.FMT_NAMES[fmt]} 4096x6656 matvec")
+    if name == "q4k_256":
+        return ([(Q4_K, 256, 6656, 0)], "single Q4_K 256x6656 matvec")
+    if name == "cat_q6k_q5k":
+        return ([(Q6_K, 512, 2560, 0), (Q5_K, 512, 2560, 1)],
+                "grid-split pair Q6_K + Q5_K 2560->512, separate x planes")
+    if name == "lm_head_q6k":
+        return ([(Q6_K, 202048, 6656, 0)], "LM head Q6_K 202048x6656")
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_bytes(members, ntok) -> int:
+    """Weights + each distinct x plane once + every y."""
+    w = sum(rows * (cols // 256) * synth.BLOCK_BYTES[f]
+            for f, rows, cols, _ in members)
+    planes = {}
+    for f, rows, cols, p in members:
+        planes[p] = cols
+    x = sum(4 * ntok * c for c in planes.values())
+    y = sum(4 * ntok * rows for _, rows, _, _ in members)
+    return w + x + y
+
+
+def host_inputs(members, ntok, label):
+    Ws = [synth.kquant_matrix(f, r, c, f"{label}/W{i}")
+          for i, (f, r, c, _) in enumerate(members)]
+    planes = {}
+    for f, r, c, p in members:
+        if p not in planes:
+            planes[p] = synth.activations(ntok, c, f"{label}/x{p}")
+    return Ws, planes
+
+
+# ----------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quant_quantized_matvec_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name, ntok):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(f"{workload_name}/ntok{ntok}")
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return int(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv",
+                                                 delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [ln.split(",") for ln in self.f.read().splitlines() if ln]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(members, Ws, planes, ntok, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on whole matrices of the
+    workload (a row sample for matrices too large to finish in budget)."""
+    import oracle
+    oracle.build()
+    done_bytes, t0, reps = 0, time.perf_counter(), 0
+    rng = np.random.default_rng(0)
+    sample_desc = None
+    while True:
+        for i, (f, r, c, p) in enumerate(members):
+            bpr = (c // 256) * synth.BLOCK_BYTES[f]
+            if r * bpr > 64 << 20:
+                idx = np.sort(rng.choice(r, size=2048, replace=False))
+                oracle.matvec(f, Ws[i], r, c, planes[p], row_idx=idx)
+                done_bytes += len(idx) * bpr + 4 * ntok * (c + len(idx))
+                sample_desc = "2048 random rows per pass"
+            else:
+                oracle.matvec(f, Ws[i], r, c, planes[p])
+                done_bytes += r * bpr + 4 * ntok * (c + r)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = done_bytes / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (sample_desc or
+                       f"{reps} full pass(es) of the workload") +
+            f", {el:.1f} s single-threaded (f32 dequant + f64 dots)"}
+
+
+# ----------------------------------------------------------------- ours
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import quant_quantized_matvec_gb300 as kq
+    from quant_quantized_matvec_gb300 import build as kbuild
+    kbuild.build()
+    kq._binding.load()
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    members, desc = workload(args.workload, args.ntok)
+    ntok = args.ntok
+    Ws, planes = host_inputs(members, ntok, f"bench/{args.workload}")
+    step_bytes = algorithmic_bytes(members, ntok)
+    w_bytes = sum(W.nbytes for W in Ws)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
+    copies = max(1, -(-3 * l2 // w_bytes)) if w_bytes < 3 * l2 else 1
+    Wd = [[torch.from_numpy(W.reshape(-1)).to(dev) for W in Ws]]
+    for _ in range(copies - 1):
+        Wd.append([w.clone() for w in Wd[0]])
+    xd = {p: torch.from_numpy(x).to(dev) for p, x in planes.items()}
+    y_all = torch.empty(sum(ntok * r for _, r, _, _ in members),
+                        dtype=torch.float32, device=dev)
+    ys, off = [], 0
+    for f, r, c, p in members:
+        ys.append(y_all[off:off + ntok * r].view(ntok, r))
+        off += ntok * r
+    sets = []
+    for cpy in Wd:
+        mem = [(f, cpy[i], r, c, xd[p], ys[i])
+               for i, (f, r, c, p) in enumerate(members)]
+        sets.append((mem, kq.make_set(mem)))
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def step(i):
+        mem, d = sets[i % len(sets)]
+        kq.matvec_set(mem, ntok=ntok, stream=stream, descriptors=d)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+
+    # CUDA graphs of L steps, replayed to make exactly K steps
+    K = args.steps
+    L = min(K, args.graph_len)
+    graphs = []
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+
+    g_main = capture(L)
+    reps, rem = K // L, K % L
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        g_main.replay()  # untimed warm replay of the graph itself
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    total_bytes = step_bytes * K * world
+    gbs = total_bytes / (ms * 1e-3) / 1e9
+    us_per_step = ms * 1e3 / K
+
+    # end to end through the public API: x from pinned host memory, outputs
+    # back to pinned host memory, every step
+    x_host = {p: torch.from_numpy(x).pin_memory() for p, x in planes.items()}
+    y_host = torch.empty(y_all.numel(), dtype=torch.float32).pin_memory()
+    Ke = min(K, args.e2e_steps)
+    h2d = sum(x.numel() * 4 for x in x_host.values())
+    d2h = y_host.numel() * 4
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(Ke):
+            for p in xd:
+                xd[p].copy_(x_host[p], non_blocking=True)
+            step(i)
+            y_host.copy_(y_all, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ems], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ems = float(t.item())
+    e2e_gbs = step_bytes * Ke * world / (ems * 1e-3) / 1e9
+
+    peak, peak_kind = peaks()
+    traffic = recorded_traffic(args.workload, ntok)
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / K, 6),
+        "us_per_call": round(us_per_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded K-quant blocks, x ~ N(0,1))",
+        "config": {
+            "workload": args.workload, "description": desc,
+            "ntok": ntok,
+            "matrices": [f"{synth.FMT_NAMES[f]} {r}x{c}"
+                         for f, r, c, _ in members],
+            "bytes_per_step": step_bytes,
+            "l2": (f"inputs rotate over {copies} weight copies "
+                   f"({copies * w_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)"
+                   if copies > 1 else
+                   f"weights {w_bytes / 1e6:.0f} MB > 3x L2"),
+            "timing": f"CUDA graphs of {L} launches, {reps} replays"
+                      + (f" + {rem}" if rem else "") + ", events on stream",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "gpu_launches": K,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(step_bytes / (ms * 1e-3 / K) / 1e9, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(step_bytes / (ms * 1e-3 / K) / 1e9 / peak, 4),
+            "traffic": traffic,
+            "peak_source": f"{peak_kind} HBM copy bandwidth",
+            "kernel": "kq_set_direct",
+        },
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(ems * 1e3 / Ke, 3), "steps": Ke,
+                "weights": "resident in HBM"},
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(members, Ws, planes, ntok,
+                                            args.cpu_budget)
+    return line
+
+
+# ----------------------------------------------------------------- reference
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step evaluates a bounded row
+    sample of the workload (rows cycle through every matrix)."""
+    import oracle
+    oracle.build()
+    members, desc = workload(args.workload, args.ntok)
+    ntok = args.ntok
+    Ws, planes = host_inputs(members, ntok, f"bench/{args.workload}")
+    rows_per_step = args.ref_rows_per_step
+    cursor = [0] * len(members)
+
+    def step():
+        nbytes = 0
+        for i, (f, r, c, p) in enumerate(members):
+            idx = (cursor[i] + np.arange(rows_per_step)) % r
+            cursor[i] = int((cursor[i] + rows_per_step) % r)
+            oracle.matvec(f, Ws[i], r, c, planes[p], row_idx=idx)
+            nbytes += len(idx) * (c // 256) * synth.BLOCK_BYTES[f] + \
+                4 * ntok * (c + len(idx))
+        return nbytes
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    total = 0
+    for _ in range(args.steps):
+        total += step()
+    el = time.perf_counter() - t0
+    gbs = total / el / 1e9
+    sample = (f"{rows_per_step} consecutive rows of each matrix per step, "
+              f"single-threaded oracle (f32 dequant + f64 dots)")
+    return {
+        "metric": METRIC, "impl": "reference",
+        "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded K-quant blocks)",
+        "config": {"workload": args.workload, "description": desc,
+                   "ntok": ntok},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qkv_gate_set")
+    ap.add_argument("--ntok", type=int, default=1)
+    ap.add_argument("--graph-len", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows-per-step", type=int, default=1)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,154 @@
+/*
+ * kq.h -- C ABI of the GB300 (sm_103a) K-quant matvec library, libkq.so.
+ *
+ * The operation ("Chapter 13 - The QKV + gate matvec family", section 13.1):
+ *
+ *     y[t][i] = sum_{j=0..cols-1} W[i,j] * x[t][j],   i < rows, t < ntok,
+ *
+ * where W is stored row-major in llama.cpp-style K-quant super-blocks of 256
+ * weights and is dequantized on the fly, never written out ("Chapter 6 - The
+ * kquant family on the reference lane", sections 6.2 and 6.4):
+ *
+ *     Q4_K  144 B / block   w = d*sc_j*nibble - dmin*m_j        (Figure 6.2)
+ *     Q5_K  176 B / block   w = d*sc_j*(nibble | hbit<<4) - dmin*m_j  (6.4)
+ *     Q6_K  210 B / block   w = d*sc_j*(code - 32), 16 int8 scales   (6.5)
+ *
+ * x and y are f32.  ntok (1..8) token columns share one read of W.
+ *
+ * Conventions for every entry point below
+ *   - Pointers to W, x and y are DEVICE pointers (cudaMalloc / torch CUDA
+ *     storage on the current device), owned by the caller.  The library
+ *     never allocates, frees or synchronizes device memory, and keeps no
+ *     pointer after a call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream) and may be captured in a CUDA graph.
+ *   - Every argument is validated on the host before anything is launched;
+ *     a call that returns an error has enqueued nothing.  KQ_ERR_CUDA means
+ *     the launch itself failed; kq_last_cuda_error() returns the CUDA error
+ *     code of the most recent such failure on the calling thread.
+ *   - Results are deterministic: a row's arithmetic depends only on the
+ *     format, cols, ntok and that row's bytes and inputs -- not on the grid,
+ *     the number of rows, or which other matrices share the launch.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Format codes: the GgmlType values of the three K-quant formats
+ * ("Chapter 6 - The kquant family on the reference lane", section 6.1). */
+typedef enum kq_fmt {
+    KQ_Q4_K = 12,
+    KQ_Q5_K = 13,
+    KQ_Q6_K = 14
+} kq_fmt;
+
+typedef enum kq_status {
+    KQ_OK = 0,
+    KQ_ERR_FORMAT = 1,  /* fmt is not one of kq_fmt                          */
+    KQ_ERR_SHAPE = 2,   /* rows < 1, cols < 256, cols % 256 != 0, or too big  */
+    KQ_ERR_NTOK = 3,    /* ntok outside 1..KQ_MAX_NTOK                        */
+    KQ_ERR_NULL = 4,    /* a required pointer is NULL                         */
+    KQ_ERR_ALIGN = 5,   /* W or x not 16-byte aligned, or y not 4-byte aligned */
+    KQ_ERR_ALIAS = 6,   /* an output overlaps an input or another output      */
+    KQ_ERR_COUNT = 7,   /* set size outside 1..KQ_MAX_SET                     */
+    KQ_ERR_CUDA = 8,    /* the CUDA launch failed (see kq_last_cuda_error)    */
+    KQ_ERR_TIMEOUT = 9  /* a bounded device-side wait expired                 */
+} kq_status;
+
+#define KQ_MAX_NTOK 8
+#define KQ_MAX_SET 16
+/* Largest accepted cols (inputs per row). */
+#define KQ_MAX_COLS (1LL << 20)
+/* Largest accepted rows per matrix. */
+#define KQ_MAX_ROWS (1LL << 30)
+
+/*
+ * Bytes per 256-weight super-block of `fmt` (144, 176 or 210; Figure 6.1 of
+ * "Chapter 6 - The kquant family on the reference lane"), or -1 if `fmt` is
+ * not a kq_fmt.  Pure host function.
+ */
+int64_t kq_block_bytes(int fmt);
+
+/*
+ * Bytes of a rows x cols matrix of `fmt`: rows * (cols/256) * block bytes,
+ * rows stored one after another with no padding (section 6.6 of the same
+ * chapter).  -1 if fmt, rows or cols is invalid.  Pure host function.
+ */
+int64_t kq_matrix_bytes(int fmt, int64_t rows, int64_t cols);
+
+/*
+ * One K-quant matvec ("Chapter 13 - The QKV + gate matvec family", sections
+ * 13.1 and 13.4; "Chapter 6", section 6.7).
+ *
+ *   fmt   kq_fmt of W.
+ *   W     device pointer, kq_matrix_bytes(fmt, rows, cols) bytes, row-major
+ *         super-blocks; 16-byte aligned.  Read only.
+ *   rows  output rows, 1..KQ_MAX_ROWS.
+ *   cols  inputs per row, a positive multiple of 256, at most KQ_MAX_COLS.
+ *   x     device pointer, f32 [ntok][cols], contiguous, 16-byte aligned.
+ *         Read only.
+ *   y     device pointer, f32 [ntok][rows], contiguous, 4-byte aligned.
+ *         Overwritten (not accumulated).  Must not overlap W or x.
+ *   ntok  token columns, 1..KQ_MAX_NTOK.
+ *   stream  cudaStream_t or NULL.
+ *
+ * Returns KQ_OK after enqueueing one kernel, or an error code with nothing
+ * enqueued (KQ_ERR_CUDA: the launch was attempted and failed).
+ */
+kq_status kq_matvec(int fmt, const void *W, int64_t rows, int64_t cols,
+                    const float *x, float *y, int ntok, void *stream);
+
+/*
+ * One member of a matvec set: a matrix, the input it reads and the output
+ * it writes.  Fields have the meaning and rules of kq_matvec's arguments.
+ */
+typedef struct kq_mat {
+    int32_t fmt;
+    int32_t reserved;   /* must be 0 */
+    const void *W;
+    int64_t rows;
+    int64_t cols;
+    const float *x;
+    float *y;
+} kq_mat;
+
+/*
+ * Several independent matvecs in ONE kernel launch, the grid split among
+ * them -- the "concurrent set" of four projections that share one read-only
+ * input and write disjoint outputs ("Chapter 13 - The QKV + gate matvec
+ * family", section 13.5), and the grid-split pair of two matrices of
+ * possibly different formats, each with its own input plane (audit note
+ * "opus_gdn_qsa", section 1, gemv_cat).
+ *
+ *   mats   host array of n kq_mat descriptors (read during the call only).
+ *   n      1..KQ_MAX_SET.
+ *   ntok   token columns shared by all members, 1..KQ_MAX_NTOK.
+ *   stream cudaStream_t or NULL.
+ *
+ * Members may differ in fmt, rows and cols; they may share x (and even W).
+ * Each y must not overlap any W, any x, or another member's y.  Each
+ * member's y is bitwise identical to what kq_matvec would write for it.
+ * Returns as kq_matvec; on error nothing is enqueued for any member.
+ */
+kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream);
+
+/* Static English text for a status code (never NULL). */
+const char *kq_status_str(int status);
+
+/* CUDA error code (cudaError_t value) of the calling thread's most recent
+ * KQ_ERR_CUDA, or 0. */
+int kq_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int kq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_H */

@@ -1,0 +1,135 @@
+"""GB300 (sm_103a) K-quant matvec: y = W x with W in Q4_K / Q5_K / Q6_K.
+
+Thin Python layer over the C ABI of libkq.so (include/kq.h).  PyTorch
+supplies device memory and streams; every step of the computation runs in
+the library's CUDA kernels.  The functions take torch CUDA tensors, check
+their dtype/shape/device, and pass raw pointers through.
+
+    import quant_quantized_matvec_gb300 as kq
+    y = kq.matvec(kq.Q4_K, W, rows, cols, x)          # x: [ntok, cols] f32
+    kq.matvec_set([(kq.Q4_K, Wq, 4096, 6656, x, yq), ...])
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _binding
+
+Q4_K, Q5_K, Q6_K = 12, 13, 14
+FORMATS = (Q4_K, Q5_K, Q6_K)
+MAX_NTOK = 8
+MAX_SET = 16
+
+
+class KQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _binding.load()
+        msg = lib.kq_status_str(status).decode()
+        extra = ""
+        if status == 8:
+            extra = f" (cudaError {lib.kq_last_cuda_error()})"
+        super().__init__(f"{where}: {_binding.STATUS.get(status, status)}: "
+                         f"{msg}{extra}")
+        self.status = status
+
+
+def _lib():
+    return _binding.load()
+
+
+def block_bytes(fmt: int) -> int:
+    return int(_lib().kq_block_bytes(int(fmt)))
+
+
+def matrix_bytes(fmt: int, rows: int, cols: int) -> int:
+    return int(_lib().kq_matrix_bytes(int(fmt), int(rows), int(cols)))
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check_tensor(t, name, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def matvec(fmt, W, rows, cols, x, y=None, stream=None):
+    """y[t, i] = sum_j W[i, j] x[t, j] for the K-quant matrix W (uint8
+    bytes, rows*(cols/256)*block_bytes of them), x [ntok, cols] or [cols]
+    f32.  Returns y [ntok, rows] (or [rows] for 1-D x), f32."""
+    import torch
+    squeeze = x.dim() == 1
+    x2 = x.unsqueeze(0) if squeeze else x
+    _check_tensor(W, "W")
+    _check_tensor(x2, "x", torch.float32)
+    ntok = x2.shape[0]
+    if x2.shape[1] != cols:
+        raise ValueError("x must have cols columns")
+    if W.numel() * W.element_size() != matrix_bytes(fmt, rows, cols):
+        raise ValueError("W size does not match fmt/rows/cols")
+    if y is None:
+        y = torch.empty((ntok, rows), dtype=torch.float32, device=x.device)
+    _check_tensor(y, "y", torch.float32)
+    if y.numel() != ntok * rows:
+        raise ValueError("y must hold ntok*rows floats")
+    st = _lib().kq_matvec(int(fmt), W.data_ptr(), int(rows), int(cols),
+                          x2.data_ptr(), y.data_ptr(), int(ntok),
+                          _stream_ptr(stream))
+    if st != 0:
+        raise KQError(st, "kq_matvec")
+    return y.view(rows) if squeeze and y.dim() == 2 and ntok == 1 else y
+
+
+def make_set(members):
+    """members: iterable of (fmt, W, rows, cols, x, y) with torch tensors.
+    Returns a ctypes array of kq_mat descriptors (reusable across calls)."""
+    members = list(members)
+    arr = (_binding.KqMat * len(members))()
+    for i, (fmt, W, rows, cols, x, y) in enumerate(members):
+        arr[i].fmt = int(fmt)
+        arr[i].reserved = 0
+        arr[i].W = W.data_ptr()
+        arr[i].rows = int(rows)
+        arr[i].cols = int(cols)
+        arr[i].x = x.data_ptr()
+        arr[i].y = y.data_ptr()
+    return arr
+
+
+def matvec_set(members, ntok=None, stream=None, descriptors=None):
+    """Several matvecs in one launch.  members: list of (fmt, W, rows, cols,
+    x, y); x [ntok, cols] f32 (members may share x), y [ntok, rows] f32.
+    `descriptors` (from make_set) skips rebuilding the descriptor array."""
+    import torch
+    members = list(members)
+    if ntok is None:
+        x0 = members[0][4]
+        ntok = 1 if x0.dim() == 1 else x0.shape[0]
+    if descriptors is None:
+        for (fmt, W, rows, cols, x, y) in members:
+            _check_tensor(W, "W")
+            _check_tensor(x, "x", torch.float32)
+            _check_tensor(y, "y", torch.float32)
+            if x.numel() != ntok * cols or y.numel() != ntok * rows:
+                raise ValueError("x / y sizes do not match ntok, rows, cols")
+            if W.numel() * W.element_size() != matrix_bytes(fmt, rows, cols):
+                raise ValueError("W size does not match fmt/rows/cols")
+        descriptors = make_set(members)
+    st = _lib().kq_matvec_set(
+        ctypes.cast(descriptors, ctypes.POINTER(_binding.KqMat)),
+        len(members), int(ntok), _stream_ptr(stream))
+    if st != 0:
+        raise KQError(st, "kq_matvec_set")
+    return [m[5] for m in members]
+

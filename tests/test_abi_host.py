@@ -1,0 +1,125 @@
+"""The C ABI on the host, without a GPU: the library loads, exports every
+function include/kq.h declares, and rejects bad arguments before it touches
+CUDA (only invalid arguments are passed here, with fake device pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quant_quantized_matvec_gb300 import _binding
+from quant_quantized_matvec_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, FORMAT, SHAPE, NTOK, NULL, ALIGN, ALIAS, COUNT = range(8)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return _binding.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kq_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert set(names) == set(_binding.SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_block_and_matrix_bytes(lib):
+    assert [lib.kq_block_bytes(f) for f in (12, 13, 14)] == [144, 176, 210]
+    assert lib.kq_block_bytes(0) == -1 and lib.kq_block_bytes(15) == -1
+    assert lib.kq_matrix_bytes(12, 4096, 6656) == 15335424
+    assert lib.kq_matrix_bytes(13, 202048, 6656) == 924571648
+    assert lib.kq_matrix_bytes(14, 202048, 6656) == 1103182080
+    assert lib.kq_matrix_bytes(12, 0, 256) == -1
+    assert lib.kq_matrix_bytes(12, 1, 255) == -1
+    assert lib.kq_matrix_bytes(12, 1, 1 << 21) == -1
+    assert lib.kq_version() >> 16 == 1
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert lib.kq_status_str(s)
+    assert lib.kq_status_str(99) == b"unknown status"
+
+
+# fake, well-aligned device addresses: validation must reject the call
+# before any CUDA call, so they are never dereferenced
+W0, X0, Y0 = 0x7f0000000000, 0x7f1000000000, 0x7f2000000000
+
+
+def mv(lib, fmt=12, W=W0, rows=64, cols=512, x=X0, y=Y0, ntok=1):
+    return lib.kq_matvec(fmt, W, rows, cols, x, y, ntok, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=11), FORMAT), (dict(fmt=0), FORMAT), (dict(fmt=1000), FORMAT),
+    (dict(rows=0), SHAPE), (dict(rows=-3), SHAPE), (dict(cols=0), SHAPE),
+    (dict(cols=255), SHAPE), (dict(cols=300), SHAPE),
+    (dict(cols=1 << 21), SHAPE), (dict(rows=(1 << 30) + 1), SHAPE),
+    (dict(ntok=0), NTOK), (dict(ntok=9), NTOK), (dict(ntok=-1), NTOK),
+    (dict(W=None), NULL), (dict(x=None), NULL), (dict(y=None), NULL),
+    (dict(W=W0 + 8), ALIGN), (dict(x=X0 + 4), ALIGN), (dict(y=Y0 + 2), ALIGN),
+    # y overlapping W, or x
+    (dict(y=W0 + 64), ALIAS), (dict(y=X0 + 1024), ALIAS),
+    (dict(y=X0 - 64), ALIAS),
+])
+def test_matvec_rejects(lib, kw, status):
+    assert mv(lib, **kw) == status
+
+
+def test_alias_edges(lib):
+    # y ending exactly where x begins does not overlap: validation passes and
+    # the call would go on to CUDA, so only the failing neighbour is checked
+    rows = 64
+    assert mv(lib, y=X0 - 4 * rows + 4) == ALIAS
+    assert mv(lib, y=W0 + 64 * 2 * 144 - 4) == ALIAS
+
+
+def _mats(specs):
+    arr = (_binding.KqMat * len(specs))()
+    for i, s in enumerate(specs):
+        d = dict(fmt=12, W=W0 + i * (1 << 28), rows=64, cols=512, x=X0,
+                 y=Y0 + i * (1 << 28), reserved=0)
+        d.update(s)
+        for k, v in d.items():
+            setattr(arr[i], k, v)
+    return arr
+
+
+def mvset(lib, specs, ntok=1, n=None):
+    arr = _mats(specs)
+    return lib.kq_matvec_set(
+        ctypes.cast(arr, ctypes.POINTER(_binding.KqMat)),
+        len(specs) if n is None else n, ntok, None)
+
+
+def test_set_rejects(lib):
+    assert mvset(lib, [{}], n=0) == COUNT
+    assert mvset(lib, [{}] * 17) == COUNT
+    assert lib.kq_matvec_set(None, 1, 1, None) == NULL
+    assert mvset(lib, [{}, {"fmt": 9}]) == FORMAT
+    assert mvset(lib, [{}, {"cols": 100}]) == SHAPE
+    assert mvset(lib, [{}, {"reserved": 1}]) == SHAPE
+    assert mvset(lib, [{}, {}], ntok=9) == NTOK
+    assert mvset(lib, [{}, {"x": None}]) == NULL
+    assert mvset(lib, [{}, {"W": W0 + 4}]) == ALIGN
+    # two outputs overlapping each other
+    assert mvset(lib, [{"y": Y0}, {"y": Y0 + 128}]) == ALIAS
+    # one member's output over another member's weights / input plane
+    assert mvset(lib, [{}, {"y": W0 + 32}]) == ALIAS
+    assert mvset(lib, [{"x": X0}, {"x": X0 + (1 << 20), "y": X0 + 16}]) == ALIAS
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _binding.load(str(tmp_path / "libkq.so"))

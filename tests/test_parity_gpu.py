@@ -1,0 +1,86 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Small cases span several CTAs and ragged tails (row counts that are not a
+multiple of the rows a CTA takes, odd block counts per row that leave Q6_K
+rows 2-byte aligned); the full-size workloads are the ones the benchmark
+times: Q4_K 256x6656; Q4_K/Q5_K/Q6_K 4096x6656 at ntok 1, 2, 4, 8 (every
+output); the 202048x6656 Q6_K LM head at ntok 1 and 4 (sampled rows).
+"""
+import numpy as np
+import pytest
+
+import gpu_cases as C
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import quant_quantized_matvec_gb300 as kq  # noqa: E402
+
+FMTS = [kq.Q4_K, kq.Q5_K, kq.Q6_K]
+NAMES = {12: "Q4_K", 13: "Q5_K", 14: "Q6_K"}
+
+
+def run(fmt, rows, cols, ntok, label, row_idx=None):
+    W, x = C.case(fmt, rows, cols, ntok, label)
+    out = C.Guarded(ntok, rows)
+    kq.matvec(fmt, C.to_dev(W), rows, cols, C.to_dev(x), y=out.y)
+    torch.cuda.synchronize()
+    y = out.host()
+    C.check(fmt, W, rows, cols, x, y, row_idx=row_idx,
+            what=f"{NAMES[fmt]} {rows}x{cols} ntok={ntok}")
+    return W, x, y
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+@pytest.mark.parametrize("ntok", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (77, 2816), (300, 768),
+                                       (33, 9472)])
+def test_small_ragged(fmt, ntok, rows, cols):
+    run(fmt, rows, cols, ntok, f"small/{fmt}/{rows}/{cols}/{ntok}")
+
+
+def test_q4k_256x6656():
+    run(kq.Q4_K, 256, 6656, 1, "cfg0")
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+@pytest.mark.parametrize("ntok", [1, 2, 4, 8])
+def test_4096x6656(fmt, ntok):
+    run(fmt, 4096, 6656, ntok, f"cfg2/{fmt}/{ntok}")
+
+
+@pytest.mark.parametrize("ntok", [1, 4])
+def test_lm_head_q6k_sampled(ntok):
+    rows, cols = 202048, 6656
+    rng = np.random.default_rng(ntok)
+    idx = np.unique(np.concatenate([
+        [0, 1, 2, 31, 32, 33, rows - 2, rows - 1],
+        rng.integers(0, rows, 400)]))
+    run(kq.Q6_K, rows, cols, ntok, f"cfg4/{ntok}", row_idx=idx)
+
+
+def test_overwrites_and_is_deterministic():
+    fmt, rows, cols, ntok = kq.Q5_K, 129, 1280, 3
+    W, x = C.case(fmt, rows, cols, ntok, "determinism")
+    Wd, xd = C.to_dev(W), C.to_dev(x)
+    a = C.Guarded(ntok, rows, fill=123.0)
+    b = C.Guarded(ntok, rows, fill=float("nan"))
+    kq.matvec(fmt, Wd, rows, cols, xd, y=a.y)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        kq.matvec(fmt, Wd, rows, cols, xd, y=b.y, stream=s)
+    torch.cuda.synchronize()
+    ya, yb = a.host(), b.host()
+    assert np.array_equal(ya.view(np.uint32), yb.view(np.uint32))
+    C.check(fmt, W, rows, cols, x, ya, what="determinism")
+
+
+def test_rejects_without_launch():
+    fmt, rows, cols = kq.Q4_K, 64, 512
+    W, x = C.case(fmt, rows, cols, 1, "reject")
+    Wd, xd = C.to_dev(W), C.to_dev(x)
+    with pytest.raises(kq.KQError, match="KQ_ERR_ALIAS"):
+        kq.matvec(fmt, Wd, rows, cols, xd, y=xd[:rows].view(1, rows))
+    with pytest.raises(kq.KQError, match="KQ_ERR_NTOK"):
+        kq.matvec(fmt, Wd, rows, cols, C.to_dev(np.zeros((9, cols),
+                                                          np.float32)))
