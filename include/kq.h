@@ -144,6 +144,29 @@ const char *kq_status_str(int status);
  * KQ_ERR_CUDA, or 0. */
 int kq_last_cuda_error(void);
 
+/*
+ * Device-side failure report.  The kernels bound every wait on a shared-
+ * memory barrier by wall time; a wait that expires sets a per-device error
+ * word (and the affected outputs to NaN) instead of hanging.  This call
+ * SYNCHRONOUSLY reads the word of the current device (a blocking device-to-
+ * host copy; it waits for work already submitted that the copy depends on)
+ * and returns KQ_ERR_TIMEOUT if it is set, KQ_OK if not.  With clear != 0 a
+ * set word is reset.  KQ_ERR_CUDA if the copy fails.
+ */
+kq_status kq_device_error(int clear);
+
+/*
+ * Kernel selection, for testing and measurement: 0 = automatic (the
+ * TMA-streaming kernel whenever the shapes can be staged in shared memory,
+ * else the direct-load kernel), 1 = always the direct-load kernel, 2 = only
+ * the streaming kernel (calls it cannot stage return KQ_ERR_SHAPE).  Both
+ * kernels compute every output with the same arithmetic in the same order,
+ * so results do not depend on this setting.  Process-wide; the environment
+ * variable KQ_KERNEL=direct|stream sets the initial value.  Returns the
+ * previous setting; an argument outside 0..2 only queries.
+ */
+int kq_select_kernel(int which);
+
 /* Library ABI version: (major << 16) | minor. */
 int kq_version(void);
 

@@ -133,3 +133,22 @@ def matvec_set(members, ntok=None, stream=None, descriptors=None):
         raise KQError(st, "kq_matvec_set")
     return [m[5] for m in members]
 
+
+
+KERNELS = {"auto": 0, "direct": 1, "stream": 2}
+
+
+def select_kernel(which: str) -> str:
+    """Choose the kernel ("auto", "direct", "stream"); returns the previous
+    choice.  Results are identical for every choice."""
+    prev = _lib().kq_select_kernel(KERNELS[which])
+    return {v: k for k, v in KERNELS.items()}[prev]
+
+
+def device_error(clear: bool = True) -> bool:
+    """True if a kernel on the current device reported an expired wait
+    (synchronous read of the device error word)."""
+    st = _lib().kq_device_error(1 if clear else 0)
+    if st == 8:
+        raise KQError(st, "kq_device_error")
+    return st == 9

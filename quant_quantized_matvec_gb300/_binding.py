@@ -18,7 +18,7 @@ STATUS = {
 }
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
-           "kq_version")
+           "kq_device_error", "kq_select_kernel", "kq_version")
 
 
 class KqMat(ctypes.Structure):
@@ -68,6 +68,10 @@ def load(path: str | None = None):
         lib.kq_status_str.restype = ctypes.c_char_p
         lib.kq_last_cuda_error.argtypes = []
         lib.kq_last_cuda_error.restype = i32
+        lib.kq_device_error.argtypes = [i32]
+        lib.kq_device_error.restype = i32
+        lib.kq_select_kernel.argtypes = [i32]
+        lib.kq_select_kernel.restype = i32
         lib.kq_version.argtypes = []
         lib.kq_version.restype = i32
         if path is None:

@@ -1,14 +1,23 @@
 // kq_api.cu -- the C ABI of libkq (include/kq.h): argument validation,
 // launch planning and the kernel launch.  Validation is pure host logic and
 // runs before any CUDA call, so a rejected call enqueues nothing.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "kq.h"
 #include "kq_kernel_direct.cuh"
+#include "kq_kernel_stream.cuh"
+
+// Device error word: set by a kernel whose bounded wait expired.
+__device__ unsigned int g_kq_device_error;
 
 namespace {
 
@@ -79,22 +88,30 @@ kq_status validate_set(const kq_mat *mats, int n, int ntok) {
 // ---------------------------------------------------------------- device
 struct DeviceInfo {
     int sms = 0;
+    int smem_optin = 0;       // dynamic shared memory a CTA may opt into
+    unsigned int *err = nullptr;  // device address of g_kq_device_error
+    bool ok = false;
 };
 
-DeviceInfo device_info(int dev) {
+// Per-device facts, looked up on the first call made with that device
+// current (that first call should come before any stream capture).
+cudaError_t device_info(int dev, DeviceInfo &out) {
     static std::mutex mu;
     static DeviceInfo cache[64];
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (cache[dev].sms == 0) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                cudaSuccess ||
-            sms <= 0)
-            sms = 148;
-        cache[dev].sms = sms;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    DeviceInfo &d = cache[dev];
+    if (!d.ok) {
+        cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaGetSymbolAddress((void **)&d.err, g_kq_device_error);
+        if (e != cudaSuccess) return e;
+        d.ok = true;
     }
-    return cache[dev];
+    out = d;
+    return cudaSuccess;
 }
 
 constexpr int kSmemLimit = 200 * 1024;
@@ -122,18 +139,9 @@ cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
     return cudaGetLastError();
 }
 
-kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
-    const kq_status v = validate_set(mats, n, ntok);
-    if (v != KQ_OK) return v;
-
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        g_last_cuda_error = (int)e;
-        return KQ_ERR_CUDA;
-    }
-    const DeviceInfo info = device_info(dev);
-
+// Plan and launch the direct-load kernel (any shape).
+kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
+                     const DeviceInfo &info) {
     kq::SetParams p{};
     p.n = n;
     int64_t grid = 0;
@@ -162,8 +170,7 @@ kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
         smem = std::max<size_t>(smem, (size_t)(per_row * rpc));
         if (grid > 0x7FFFFFFF) return KQ_ERR_SHAPE;
     }
-
-    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
     switch (ntok) {
     case 1: e = launch_direct<1>(p, (int)grid, smem, s); break;
     case 2: e = launch_direct<2>(p, (int)grid, smem, s); break;
@@ -179,6 +186,284 @@ kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
         return KQ_ERR_CUDA;
     }
     return KQ_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)f;
+    });
+    return fn;
+}
+
+struct MapKey {
+    uintptr_t W;
+    int64_t rows, row_bytes;
+    int box_w, box_h;
+    bool operator==(const MapKey &o) const {
+        return W == o.W && rows == o.rows && row_bytes == o.row_bytes && box_w == o.box_w &&
+               box_h == o.box_h;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const {
+        size_t h = (size_t)k.W * 0x9E3779B97F4A7C15ull;
+        h ^= (size_t)k.rows + 0x1234567 + (h << 6) + (h >> 2);
+        h ^= (size_t)k.row_bytes + (h << 6) + (h >> 2);
+        h ^= (size_t)(k.box_w * 977 + k.box_h) + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+
+// A 2-D map over a row-major byte matrix viewed as [rows][row_bytes/8] u64,
+// box [box_h rows][box_w u64]; boxes past the last column are zero-filled.
+// Encoded maps are cached by (W, shape, box): encoding is a host-only call.
+bool tensor_map(const void *W, int64_t rows, int64_t row_bytes, int box_w, int box_h,
+                CUtensorMap *out) {
+    static std::mutex mu;
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    const MapKey key{(uintptr_t)W, rows, row_bytes, box_w, box_h};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *out = it->second;
+            return true;
+        }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    CUtensorMap m;
+    cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)box_w, (cuuint32_t)box_h};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache.emplace(key, m);
+    *out = m;
+    return true;
+}
+
+template <int NTOK, bool XSMEM>
+cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cudaStream_t s) {
+    static std::mutex mu;
+    static size_t configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev] < smem) {
+            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = smem;
+        }
+    }
+    kq::kq_set_stream<NTOK, XSMEM><<<grid, kq::kStreamThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <bool XSMEM>
+cudaError_t launch_stream_ntok(int ntok, const kq::StreamParams &p, int grid, size_t smem,
+                               cudaStream_t s) {
+    switch (ntok) {
+    case 1: return launch_stream<1, XSMEM>(p, grid, smem, s);
+    case 2: return launch_stream<2, XSMEM>(p, grid, smem, s);
+    case 3: return launch_stream<3, XSMEM>(p, grid, smem, s);
+    case 4: return launch_stream<4, XSMEM>(p, grid, smem, s);
+    case 5: return launch_stream<5, XSMEM>(p, grid, smem, s);
+    case 6: return launch_stream<6, XSMEM>(p, grid, smem, s);
+    case 7: return launch_stream<7, XSMEM>(p, grid, smem, s);
+    default: return launch_stream<8, XSMEM>(p, grid, smem, s);
+    }
+}
+
+int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// Plan the streaming kernel.  Returns KQ_OK after launching, or
+// KQ_ERR_SHAPE when the shapes cannot be staged (caller falls back).
+kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
+                     const DeviceInfo &info, bool *launched) {
+    *launched = false;
+    static kq::StreamParams p;  // ~10 KB: kept off the stack
+    static std::mutex pmu;
+    std::lock_guard<std::mutex> plock(pmu);
+    memset(&p, 0, sizeof(p));
+    p.n = n;
+    const int G = info.sms;
+
+    // CTAs per member in proportion to its bytes (at least one, at most one
+    // per row), largest remainder first.
+    int64_t bytes[KQ_MAX_SET], total = 0;
+    for (int i = 0; i < n; ++i) {
+        bytes[i] = mats[i].rows * (mats[i].cols / 256) * block_bytes_of(mats[i].fmt);
+        total += bytes[i];
+    }
+    int ncta[KQ_MAX_SET];
+    double rem[KQ_MAX_SET];
+    int used = 0;
+    for (int i = 0; i < n; ++i) {
+        const double share = (double)G * (double)bytes[i] / (double)total;
+        ncta[i] = std::max(1, (int)share);
+        rem[i] = share - (int)share;
+        ncta[i] = (int)std::min<int64_t>(ncta[i], mats[i].rows);
+        used += ncta[i];
+    }
+    while (used < G) {
+        int best = -1;
+        for (int i = 0; i < n; ++i)
+            if (ncta[i] < mats[i].rows && (best < 0 || rem[i] > rem[best])) best = i;
+        if (best < 0) break;
+        ++ncta[best];
+        rem[best] = -1.0;
+        ++used;
+    }
+    while (used > G) {  // only when n > G
+        int best = 0;
+        for (int i = 1; i < n; ++i)
+            if (ncta[i] > ncta[best]) best = i;
+        if (ncta[best] <= 1) break;
+        --ncta[best];
+        --used;
+    }
+
+    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0;
+    int cta = 0;
+    for (int i = 0; i < n; ++i) {
+        const kq_mat &m = mats[i];
+        kq::StreamMember &M = p.m[i];
+        const int nb = (int)(m.cols / 256);
+        const int bb = (int)block_bytes_of(m.fmt);
+        const int64_t row_bytes = (int64_t)nb * bb;
+        M.W = (const uint8_t *)m.W;
+        M.x = m.x;
+        M.y = m.y;
+        M.rows = m.rows;
+        M.nb = nb;
+        M.fmt = m.fmt;
+        M.cta_begin = cta;
+        M.ncta = ncta[i];
+        cta += ncta[i];
+        // rows per group: partials for the group must fit in 64 KiB
+        const int64_t part_row = (int64_t)nb * ntok * 4;
+        int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, 32);
+        if (m.fmt == KQ_Q6_K)
+            rmax = (int)std::min<int64_t>(rmax, std::min<int64_t>(16, (65536 - 32) / row_bytes));
+        if (rmax < 1) return KQ_ERR_SHAPE;
+        M.rmax = rmax;
+        M.kb = nb < 7 ? nb : 7;
+        // group heights that occur: n in {floor, ceil}(rows / ncta)
+        int hs[kq::kMaxMaps], nh = 0, hmax = 0;
+        const int64_t nlo = m.rows / ncta[i], nhi = (m.rows + ncta[i] - 1) / ncta[i];
+        for (int64_t nn = nlo; nn <= nhi; ++nn) {
+            if (nn < 1) continue;
+            const int64_t ng = (nn + rmax - 1) / rmax;
+            for (int64_t hh = nn / ng; hh <= (nn + ng - 1) / ng; ++hh) {
+                bool seen = false;
+                for (int j = 0; j < nh; ++j) seen |= hs[j] == hh;
+                if (!seen) {
+                    if (nh == kq::kMaxMaps) return KQ_ERR_SHAPE;
+                    hs[nh++] = (int)hh;
+                }
+                hmax = std::max<int>(hmax, (int)hh);
+            }
+        }
+        M.nmaps = m.fmt == KQ_Q6_K ? 0 : nh;
+        if (m.fmt != KQ_Q6_K) {
+            const int box_w = (int)(M.kb * bb / 8);
+            for (int j = 0; j < nh; ++j) {
+                M.map_h[j] = hs[j];
+                if (!tensor_map(m.W, m.rows, row_bytes, box_w, hs[j], &p.maps[i][j]))
+                    return KQ_ERR_SHAPE;
+            }
+            slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * M.kb * bb);
+        } else {
+            slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * row_bytes + 32);
+        }
+        x_bytes = std::max<int64_t>(x_bytes, (int64_t)ntok * m.cols * 4);
+        part_bytes = std::max<int64_t>(part_bytes, (int64_t)hmax * part_row);
+    }
+    const bool xsmem = x_bytes <= 64 * 1024;
+    if (!xsmem) x_bytes = 0;
+    part_bytes = round_up(part_bytes, 128);
+    slot_bytes = round_up(slot_bytes, 128);
+    const int64_t fixed = 1024 + x_bytes + part_bytes;
+    // the 1 KiB alignment of the dynamic region pads the static part to 1 KiB
+    const int64_t budget = (int64_t)info.smem_optin - 1024;
+    const int64_t nslot = std::min<int64_t>(kq::kMaxSlots, (budget - fixed) / slot_bytes);
+    if (nslot < 2) return KQ_ERR_SHAPE;
+    p.nslot = (int)nslot;
+    p.slot_bytes = (int)slot_bytes;
+    p.x_bytes = (int)x_bytes;
+    p.part_bytes = (int)part_bytes;
+    p.err = info.err;
+    const size_t smem = (size_t)(fixed + nslot * slot_bytes);
+    const cudaError_t e = xsmem ? launch_stream_ntok<true>(ntok, p, cta, smem, s)
+                                : launch_stream_ntok<false>(ntok, p, cta, smem, s);
+    *launched = true;
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    return KQ_OK;
+}
+
+// Kernel choice: the streaming kernel when the shapes can be staged, else
+// the direct-load kernel.  KQ_KERNEL=direct|stream forces one (testing and
+// measurement only; both give bitwise identical results).
+std::atomic<int> g_choice{-1};
+
+int kernel_choice() {
+    int c = g_choice.load();
+    if (c < 0) {
+        const char *e = getenv("KQ_KERNEL");
+        c = (e && !strcmp(e, "direct")) ? 1 : (e && !strcmp(e, "stream")) ? 2 : 0;
+        int expected = -1;
+        g_choice.compare_exchange_strong(expected, c);
+        c = g_choice.load();
+    }
+    return c;
+}
+
+kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
+    const kq_status v = validate_set(mats, n, ntok);
+    if (v != KQ_OK) return v;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    DeviceInfo info;
+    if (e == cudaSuccess) e = device_info(dev, info);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const int choice = kernel_choice();
+    if (choice != 1) {
+        bool launched = false;
+        const kq_status st = run_stream(mats, n, ntok, s, info, &launched);
+        if (launched || choice == 2) return st;
+    }
+    return run_direct(mats, n, ntok, s, info);
 }
 
 }  // namespace
@@ -229,6 +514,30 @@ const char *kq_status_str(int status) {
 }
 
 int kq_last_cuda_error(void) { return g_last_cuda_error; }
+
+kq_status kq_device_error(int clear) {
+    int dev = 0;
+    DeviceInfo info;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = device_info(dev, info);
+    unsigned int v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, info.err, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear && v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(info.err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    }
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    return v ? KQ_ERR_TIMEOUT : KQ_OK;
+}
+
+int kq_select_kernel(int which) {
+    const int prev = kernel_choice();
+    if (which >= 0 && which <= 2) g_choice.store(which);
+    return prev;
+}
 
 int kq_version(void) { return (1 << 16) | 0; }
 

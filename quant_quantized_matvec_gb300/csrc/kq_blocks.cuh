@@ -1,7 +1,8 @@
 // kq_blocks.cuh -- one super-block of one row against ntok inputs.
 //
-// Each function takes the block's bytes (already in registers), a pointer to
-// the 256 inputs the block multiplies (token plane stride `xs`), and returns
+// Each function takes the block's bytes (already in registers), an accessor
+// for the 256 inputs the block multiplies (x.ld(t, e) returns inputs e..e+3
+// of token t, relative to the block's first input), and returns
 // the block's contribution to each token's dot product.  The arithmetic is a
 // fixed function of the block bytes and the inputs: every weight is first
 // dequantized exactly as "Chapter 6 - The kquant family on the reference
@@ -30,10 +31,9 @@ __device__ __forceinline__ void finish(float (&acc)[NTOK][4],
 // bytes 32g..32g+31: the low nibble of byte 32g+l is weight 64g+l, the high
 // nibble weight 64g+32+l.  Q5_K's fifth bit of those two weights is bit 2g,
 // resp. 2g+1, of qh[l].
-template <int NTOK, bool Q5>
+template <int NTOK, bool Q5, class XA>
 __device__ __forceinline__ void block_q45(const uint4 (&blk)[Q5 ? 11 : 9],
-                                          const float *__restrict__ x,
-                                          int64_t xs, float (&part)[NTOK]) {
+                                          const XA &x, float (&part)[NTOK]) {
     constexpr int QS = Q5 ? 3 : 1;  // first uint4 of qs
     const float d = h2f(blk[0].x), dmin = h2f(blk[0].x >> 16);
     const ScaleWords sw = unpack_scale_words(blk[0].y, blk[0].z, blk[0].w);
@@ -69,8 +69,8 @@ __device__ __forceinline__ void block_q45(const uint4 (&blk)[Q5 ? 11 : 9],
             }
 #pragma unroll
             for (int t = 0; t < NTOK; ++t) {
-                const float4 xl = ldg_f4(x + t * xs + 64 * g + 4 * k);
-                const float4 xh = ldg_f4(x + t * xs + 64 * g + 32 + 4 * k);
+                const float4 xl = x.ld(t, 64 * g + 4 * k);
+                const float4 xh = x.ld(t, 64 * g + 32 + 4 * k);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     acc[t][i] = fmaf(wl[i], comp(xl, i), acc[t][i]);
@@ -89,10 +89,9 @@ __device__ __forceinline__ void block_q45(const uint4 (&blk)[Q5 ? 11 : 9],
 // take the low nibble of ql[64h+l], the low nibble of ql[64h+32+l], the high
 // nibble of ql[64h+l], the high nibble of ql[64h+32+l], and the bit pairs
 // 0-1, 2-3, 4-5, 6-7 of qh[32h+l].  Weight = d*sc[e/16]*(code-32): exact.
-template <int NTOK>
+template <int NTOK, class XA>
 __device__ __forceinline__ void block_q6(const uint32_t (&L)[52], uint32_t dbits,
-                                         const float *__restrict__ x,
-                                         int64_t xs, float (&part)[NTOK]) {
+                                         const XA &x, float (&part)[NTOK]) {
     const float d = h2f(dbits);
     float scl[16];
 #pragma unroll
@@ -129,7 +128,7 @@ __device__ __forceinline__ void block_q6(const uint32_t (&L)[52], uint32_t dbits
                                 8388640.0f);  // code - 32, exact
 #pragma unroll
                 for (int t = 0; t < NTOK; ++t) {
-                    const float4 xv = ldg_f4(x + t * xs + e0);
+                    const float4 xv = x.ld(t, e0);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         acc[t][i] = fmaf(w[i], comp(xv, i), acc[t][i]);

@@ -68,6 +68,26 @@ __device__ __forceinline__ float4 ldg_f4(const float *p) {
     return __ldg(reinterpret_cast<const float4 *>(p));
 }
 
+// Input accessors for kq_blocks.cuh: x.ld(t, e) = inputs e..e+3 of token t.
+struct XGlobal {  // read-only global loads (L1-cached)
+    const float *p;
+    int64_t plane;  // floats between token planes
+    __device__ __forceinline__ float4 ld(int t, int e) const {
+        return ldg_f4(p + t * plane + e);
+    }
+};
+struct XShared {  // shared-memory copy of x
+    uint32_t a;     // shared address of this block's first input, token 0
+    uint32_t plane; // bytes between token planes
+    __device__ __forceinline__ float4 ld(int t, int e) const {
+        float4 v;
+        asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                     : "r"(a + t * plane + 4 * e));
+        return v;
+    }
+};
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
     return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
 }

@@ -58,24 +58,24 @@ __global__ void __launch_bounds__(kDirectThreads)
         const int b = task / R;
         const int r = task - b * R;
         const int64_t blk_index = (r0 + r) * nb + b;
-        const float *xb = M.x + (int64_t)b * 256;
+        const XGlobal xb{M.x + (int64_t)b * 256, cols};
         float part[NTOK];
         if (M.fmt == kFmtQ4K) {
             const uint8_t *a = M.W + blk_index * 144;
             uint4 v[9];
 #pragma unroll
             for (int i = 0; i < 9; ++i) v[i] = ldg_v4(a + 16 * i);
-            block_q45<NTOK, false>(v, xb, cols, part);
+            block_q45<NTOK, false>(v, xb, part);
         } else if (M.fmt == kFmtQ5K) {
             const uint8_t *a = M.W + blk_index * 176;
             uint4 v[11];
 #pragma unroll
             for (int i = 0; i < 11; ++i) v[i] = ldg_v4(a + 16 * i);
-            block_q45<NTOK, true>(v, xb, cols, part);
+            block_q45<NTOK, true>(v, xb, part);
         } else {
             uint32_t L[52], dbits;
             load_q6(M.W + blk_index * 210, L, dbits);
-            block_q6<NTOK>(L, dbits, xb, cols, part);
+            block_q6<NTOK>(L, dbits, xb, part);
         }
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) part_s[(b * R + r) * NTOK + t] = part[t];

@@ -80,7 +80,32 @@ def test_rejects_without_launch():
     W, x = C.case(fmt, rows, cols, 1, "reject")
     Wd, xd = C.to_dev(W), C.to_dev(x)
     with pytest.raises(kq.KQError, match="KQ_ERR_ALIAS"):
-        kq.matvec(fmt, Wd, rows, cols, xd, y=xd[:rows].view(1, rows))
+        kq.matvec(fmt, Wd, rows, cols, xd, y=xd.view(-1)[:rows].view(1, rows))
     with pytest.raises(kq.KQError, match="KQ_ERR_NTOK"):
         kq.matvec(fmt, Wd, rows, cols, C.to_dev(np.zeros((9, cols),
                                                           np.float32)))
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+@pytest.mark.parametrize("ntok", [1, 2, 5, 8])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (77, 2816), (300, 768),
+                                       (33, 9472), (4096, 6656)])
+def test_stream_equals_direct(fmt, ntok, rows, cols):
+    """The TMA-streaming kernel and the direct-load kernel compute each
+    output with the same arithmetic in the same order: bitwise equal."""
+    W, x = C.case(fmt, rows, cols, ntok, f"kern/{fmt}/{rows}/{cols}/{ntok}")
+    Wd, xd = C.to_dev(W), C.to_dev(x)
+    outs = {}
+    try:
+        for k in ("direct", "stream"):
+            kq.select_kernel(k)
+            g = C.Guarded(ntok, rows)
+            kq.matvec(fmt, Wd, rows, cols, xd, y=g.y)
+            torch.cuda.synchronize()
+            outs[k] = g.host()
+    finally:
+        kq.select_kernel("auto")
+    assert not kq.device_error()
+    assert np.array_equal(outs["direct"].view(np.uint32),
+                          outs["stream"].view(np.uint32))
+    C.check(fmt, W, rows, cols, x, outs["stream"], what="stream kernel")
