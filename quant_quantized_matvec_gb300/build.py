@@ -42,18 +42,36 @@ def is_stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not is_stale():
-        return LIB
-    os.makedirs(os.path.dirname(LIB), exist_ok=True)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-           "-o", tmp, *sources()]
+def _compile(args):
+    src, obj, verbose = args
+    cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+           "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    return src, r.returncode, r.stdout + r.stderr
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every .cu under csrc/ in parallel, then link libkq.so."""
+    if not force and not is_stale():
+        return LIB
+    from concurrent.futures import ThreadPoolExecutor
+    objdir = os.path.join(PKG, "lib", "obj")
+    os.makedirs(objdir, exist_ok=True)
+    jobs = [(src, os.path.join(objdir, os.path.basename(src) + ".o"), verbose)
+            for src in sources()]
+    with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(_compile, jobs))
+    failed = [(s, out) for s, rc, out in results if rc != 0]
+    for s, rc, out in results:
+        if verbose or rc != 0:
+            print(out, end="", flush=True)
+    if failed:
+        raise RuntimeError("nvcc failed for " + ", ".join(s for s, _ in failed))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.run([nvcc(), ARCH, "-shared", "-o", tmp] + [j[1] for j in jobs],
+                   check=True)
     os.replace(tmp, LIB)
     return LIB
 

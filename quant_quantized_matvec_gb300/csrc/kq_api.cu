@@ -13,8 +13,52 @@
 #include <unordered_map>
 
 #include "kq.h"
-#include "kq_kernel_direct.cuh"
-#include "kq_kernel_stream.cuh"
+#include "kq_launch.cuh"
+
+KQ_DECLARE_INSTANCES(1)
+KQ_DECLARE_INSTANCES(2)
+KQ_DECLARE_INSTANCES(3)
+KQ_DECLARE_INSTANCES(4)
+KQ_DECLARE_INSTANCES(5)
+KQ_DECLARE_INSTANCES(6)
+KQ_DECLARE_INSTANCES(7)
+KQ_DECLARE_INSTANCES(8)
+
+namespace kqlaunch {
+cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s) {
+    switch (ntok) {
+    case 1: return launch_direct<1>(p, grid, smem, s);
+    case 2: return launch_direct<2>(p, grid, smem, s);
+    case 3: return launch_direct<3>(p, grid, smem, s);
+    case 4: return launch_direct<4>(p, grid, smem, s);
+    case 5: return launch_direct<5>(p, grid, smem, s);
+    case 6: return launch_direct<6>(p, grid, smem, s);
+    case 7: return launch_direct<7>(p, grid, smem, s);
+    default: return launch_direct<8>(p, grid, smem, s);
+    }
+}
+cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
+                   cudaStream_t s) {
+    switch (ntok * 2 + (xsmem ? 1 : 0)) {
+    case 3: return launch_stream<1, true>(p, grid, smem, s);
+    case 2: return launch_stream<1, false>(p, grid, smem, s);
+    case 5: return launch_stream<2, true>(p, grid, smem, s);
+    case 4: return launch_stream<2, false>(p, grid, smem, s);
+    case 7: return launch_stream<3, true>(p, grid, smem, s);
+    case 6: return launch_stream<3, false>(p, grid, smem, s);
+    case 9: return launch_stream<4, true>(p, grid, smem, s);
+    case 8: return launch_stream<4, false>(p, grid, smem, s);
+    case 11: return launch_stream<5, true>(p, grid, smem, s);
+    case 10: return launch_stream<5, false>(p, grid, smem, s);
+    case 13: return launch_stream<6, true>(p, grid, smem, s);
+    case 12: return launch_stream<6, false>(p, grid, smem, s);
+    case 15: return launch_stream<7, true>(p, grid, smem, s);
+    case 14: return launch_stream<7, false>(p, grid, smem, s);
+    case 17: return launch_stream<8, true>(p, grid, smem, s);
+    default: return launch_stream<8, false>(p, grid, smem, s);
+    }
+}
+}  // namespace kqlaunch
 
 // Device error word: set by a kernel whose bounded wait expired.
 __device__ unsigned int g_kq_device_error;
@@ -114,30 +158,7 @@ cudaError_t device_info(int dev, DeviceInfo &out) {
     return cudaSuccess;
 }
 
-constexpr int kSmemLimit = 200 * 1024;
-
-template <int NTOK>
-cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
-                          cudaStream_t stream) {
-    static std::mutex mu;
-    static size_t configured[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (smem > 48 * 1024) {
-        std::lock_guard<std::mutex> lock(mu);
-        if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(kq::kq_set_direct<NTOK>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemLimit);
-            if (e != cudaSuccess) return e;
-            configured[dev] = kSmemLimit;
-        }
-    }
-    kq::kq_set_direct<NTOK><<<grid, kq::kDirectThreads, smem, stream>>>(p);
-    return cudaGetLastError();
-}
+constexpr int kSmemLimit = kqlaunch::kDirectSmemLimit;
 
 // Plan and launch the direct-load kernel (any shape).
 kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
@@ -170,17 +191,7 @@ kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         smem = std::max<size_t>(smem, (size_t)(per_row * rpc));
         if (grid > 0x7FFFFFFF) return KQ_ERR_SHAPE;
     }
-    cudaError_t e;
-    switch (ntok) {
-    case 1: e = launch_direct<1>(p, (int)grid, smem, s); break;
-    case 2: e = launch_direct<2>(p, (int)grid, smem, s); break;
-    case 3: e = launch_direct<3>(p, (int)grid, smem, s); break;
-    case 4: e = launch_direct<4>(p, (int)grid, smem, s); break;
-    case 5: e = launch_direct<5>(p, (int)grid, smem, s); break;
-    case 6: e = launch_direct<6>(p, (int)grid, smem, s); break;
-    case 7: e = launch_direct<7>(p, (int)grid, smem, s); break;
-    default: e = launch_direct<8>(p, (int)grid, smem, s); break;
-    }
+    const cudaError_t e = kqlaunch::direct(ntok, p, (int)grid, smem, s);
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
@@ -261,42 +272,6 @@ bool tensor_map(const void *W, int64_t rows, int64_t row_bytes, int box_w, int b
     return true;
 }
 
-template <int NTOK, bool XSMEM>
-cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cudaStream_t s) {
-    static std::mutex mu;
-    static size_t configured[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) dev = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            configured[dev] = smem;
-        }
-    }
-    kq::kq_set_stream<NTOK, XSMEM><<<grid, kq::kStreamThreads, smem, s>>>(p);
-    return cudaGetLastError();
-}
-
-template <bool XSMEM>
-cudaError_t launch_stream_ntok(int ntok, const kq::StreamParams &p, int grid, size_t smem,
-                               cudaStream_t s) {
-    switch (ntok) {
-    case 1: return launch_stream<1, XSMEM>(p, grid, smem, s);
-    case 2: return launch_stream<2, XSMEM>(p, grid, smem, s);
-    case 3: return launch_stream<3, XSMEM>(p, grid, smem, s);
-    case 4: return launch_stream<4, XSMEM>(p, grid, smem, s);
-    case 5: return launch_stream<5, XSMEM>(p, grid, smem, s);
-    case 6: return launch_stream<6, XSMEM>(p, grid, smem, s);
-    case 7: return launch_stream<7, XSMEM>(p, grid, smem, s);
-    default: return launch_stream<8, XSMEM>(p, grid, smem, s);
-    }
-}
-
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 // Plan the streaming kernel.  Returns KQ_OK after launching, or
@@ -346,7 +321,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         --used;
     }
 
-    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0;
+    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0, raw_x = 0;
     int cta = 0;
     for (int i = 0; i < n; ++i) {
         const kq_mat &m = mats[i];
@@ -370,7 +345,24 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
             rmax = (int)std::min<int64_t>(rmax, std::min<int64_t>(16, (65536 - 32) / row_bytes));
         if (rmax < 1) return KQ_ERR_SHAPE;
         M.rmax = rmax;
-        M.kb = nb < 7 ? nb : 7;
+        // Blocks per box: a box row is at most 2048 bytes (256 u64); prefer
+        // few boxes per row, then no zero-filled tail, then an odd number
+        // of 16-byte units per row (rows on distinct shared-memory banks).
+        {
+            const int kbmax = (int)std::min<int64_t>(nb, 2048 / bb);
+            int best = 1;
+            int64_t best_key = INT64_MAX;
+            for (int kb = 1; kb <= kbmax; ++kb) {
+                const int64_t nbox = (nb + kb - 1) / kb, waste = nbox * kb - nb;
+                const int64_t units = (int64_t)kb * bb / 16;
+                const int64_t key = nbox * 1000000 + waste * 10 + ((units & 1) ? 0 : 1);
+                if (key < best_key) {
+                    best_key = key;
+                    best = kb;
+                }
+            }
+            M.kb = best;
+        }
         // group heights that occur: n in {floor, ceil}(rows / ncta)
         int hs[kq::kMaxMaps], nh = 0, hmax = 0;
         const int64_t nlo = m.rows / ncta[i], nhi = (m.rows + ncta[i] - 1) / ncta[i];
@@ -399,12 +391,18 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         } else {
             slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * row_bytes + 32);
         }
-        x_bytes = std::max<int64_t>(x_bytes, (int64_t)ntok * m.cols * 4);
+        // scaled inputs [ntok][nb][260] (a 16-byte pad per block) and
+        // sub-block sums [ntok][cols/32]
+        x_bytes = std::max<int64_t>(
+            x_bytes, round_up((int64_t)ntok * nb * 260 * 4 + (int64_t)ntok * m.cols / 8, 128));
+        raw_x = std::max<int64_t>(raw_x, (int64_t)ntok * m.cols * 4);
         part_bytes = std::max<int64_t>(part_bytes, (int64_t)hmax * part_row);
     }
-    const bool xsmem = x_bytes <= 64 * 1024;
+    const bool xsmem = x_bytes <= 72 * 1024;
     if (!xsmem) x_bytes = 0;
-    part_bytes = round_up(part_bytes, 128);
+    // with inputs in shared memory the raw copy is staged in a ring slot
+    if (xsmem) slot_bytes = std::max(slot_bytes, raw_x);
+    part_bytes = 2 * round_up(part_bytes, 128);  // two row groups in flight
     slot_bytes = round_up(slot_bytes, 128);
     const int64_t fixed = 1024 + x_bytes + part_bytes;
     // the 1 KiB alignment of the dynamic region pads the static part to 1 KiB
@@ -417,8 +415,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.part_bytes = (int)part_bytes;
     p.err = info.err;
     const size_t smem = (size_t)(fixed + nslot * slot_bytes);
-    const cudaError_t e = xsmem ? launch_stream_ntok<true>(ntok, p, cta, smem, s)
-                                : launch_stream_ntok<false>(ntok, p, cta, smem, s);
+    const cudaError_t e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s);
     *launched = true;
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;

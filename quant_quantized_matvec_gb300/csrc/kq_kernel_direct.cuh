@@ -6,7 +6,8 @@
 // read the same inputs.  Every thread loads its super-block straight from
 // global memory with 16-byte (Q4_K, Q5_K) or 4-byte (Q6_K, whose 210-byte
 // blocks are only 2-byte aligned) read-only loads, computes the block's
-// contribution to each token (kq_blocks.cuh), and parks it in shared memory.
+// contribution to each token (kq_blocks.cuh; inputs are read from global
+// memory and scaled on the fly), and parks it in shared memory.
 // After one barrier each (row, token) sums its blocks in block order 0..nb-1
 // and writes y.  The sum order depends on nothing but nb, so a member's
 // output is the same whichever set, grid or row split it runs in.
@@ -17,25 +18,6 @@
 namespace kq {
 
 constexpr int kDirectThreads = 256;
-
-// Load one Q6_K block at byte address a (2-byte aligned) as 52 words of
-// block bytes 4k..4k+3 plus the f16 d, without touching bytes outside the
-// block except the two before it when a is 2 mod 4 (they belong to the
-// previous block of the same matrix, which exists because the matrix start
-// is 16-byte aligned).
-__device__ __forceinline__ void load_q6(const uint8_t *a, uint32_t (&L)[52],
-                                        uint32_t &dbits) {
-    const uint32_t mis = (uint32_t)((uintptr_t)a & 3u);  // 0 or 2
-    const uint8_t *base = a - mis;
-    const uint32_t s = mis * 8u;
-    uint32_t raw[53];
-#pragma unroll
-    for (int k = 0; k < 52; ++k) raw[k] = ldg_u32(base + 4 * k);
-    raw[52] = mis ? ldg_u32(base + 208) : ldg_u16(base + 208);
-#pragma unroll
-    for (int k = 0; k < 52; ++k) L[k] = __funnelshift_r(raw[k], raw[k + 1], s);
-    dbits = (raw[52] >> s) & 0xFFFFu;
-}
 
 template <int NTOK>
 __global__ void __launch_bounds__(kDirectThreads)
@@ -58,24 +40,26 @@ __global__ void __launch_bounds__(kDirectThreads)
         const int b = task / R;
         const int r = task - b * R;
         const int64_t blk_index = (r0 + r) * nb + b;
-        const XGlobal xb{M.x + (int64_t)b * 256, cols};
+        const float *xb = M.x + (int64_t)b * 256;
         float part[NTOK];
         if (M.fmt == kFmtQ4K) {
-            const uint8_t *a = M.W + blk_index * 144;
-            uint4 v[9];
+            const BlockGlobal B[1] = {{reinterpret_cast<const uint4 *>(M.W + blk_index * 144)}};
+            float p1[1][NTOK];
+            block_q45<NTOK, false, 1>(B, XGlobalS<true>{xb, cols}, p1);
 #pragma unroll
-            for (int i = 0; i < 9; ++i) v[i] = ldg_v4(a + 16 * i);
-            block_q45<NTOK, false>(v, xb, part);
+            for (int t = 0; t < NTOK; ++t) part[t] = p1[0][t];
         } else if (M.fmt == kFmtQ5K) {
-            const uint8_t *a = M.W + blk_index * 176;
-            uint4 v[11];
+            const BlockGlobal B[1] = {{reinterpret_cast<const uint4 *>(M.W + blk_index * 176)}};
+            float p1[1][NTOK];
+            block_q45<NTOK, true, 1>(B, XGlobalS<false>{xb, cols}, p1);
 #pragma unroll
-            for (int i = 0; i < 11; ++i) v[i] = ldg_v4(a + 16 * i);
-            block_q45<NTOK, true>(v, xb, part);
+            for (int t = 0; t < NTOK; ++t) part[t] = p1[0][t];
         } else {
-            uint32_t L[52], dbits;
-            load_q6(M.W + blk_index * 210, L, dbits);
-            block_q6<NTOK>(L, dbits, xb, part);
+            const uint8_t *a = M.W + blk_index * 210;
+            if ((uintptr_t)a & 3u)
+                block_q6k<NTOK>(Q6GlobalShifted{a - 2}, XGlobalS<false>{xb, cols}, part);
+            else
+                block_q6k<NTOK>(Q6GlobalAligned{a}, XGlobalS<false>{xb, cols}, part);
         }
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) part_s[(b * R + r) * NTOK + t] = part[t];

@@ -32,7 +32,7 @@
 
 namespace kq {
 
-constexpr int kStreamConsumers = 8;
+constexpr int kStreamConsumers = 12;
 constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
 constexpr int kMaxMaps = 4;
 constexpr int kMaxSlots = 32;
@@ -83,7 +83,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 100000;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -123,34 +123,32 @@ __device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap *ma
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kStreamConsumers * 32) : "memory");
 }
-__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
 
-// A Q6_K block at shared address a (2-byte aligned) as 52 words + d.  Reads
-// the two bytes before the block when a is 2 mod 4 and the two after it
-// otherwise; both stay inside the stage's slot.
-__device__ __forceinline__ void lds_q6(uint32_t a, uint32_t (&L)[52],
-                                       uint32_t &dbits) {
-    const uint32_t mis = a & 3u;
-    const uint32_t base = a - mis;
-    const uint32_t s = mis * 8u;
-    uint32_t raw[53];
+
+// Word sources for Q6_K blocks staged in shared memory (kq_blocks.cuh).
+struct Q6SharedAligned {
+    const uint8_t *a;
+    __device__ __forceinline__ void words4(int j, uint32_t (&o)[4]) const {
 #pragma unroll
-    for (int k = 0; k < 53; ++k) raw[k] = lds_u32(base + 4 * k);
+        for (int i = 0; i < 4; ++i) o[i] = *reinterpret_cast<const uint32_t *>(a + 4 * (j + i));
+    }
+    __device__ __forceinline__ uint32_t dbits() const {
+        return *reinterpret_cast<const uint16_t *>(a + 208);
+    }
+};
+struct Q6SharedShifted {  // a = block start - 2 (4-byte aligned)
+    const uint8_t *a;
+    __device__ __forceinline__ void words4(int j, uint32_t (&o)[4]) const {
+        uint32_t r[5];
 #pragma unroll
-    for (int k = 0; k < 52; ++k) L[k] = __funnelshift_r(raw[k], raw[k + 1], s);
-    dbits = (raw[52] >> s) & 0xFFFFu;
-}
+        for (int i = 0; i < 5; ++i) r[i] = *reinterpret_cast<const uint32_t *>(a + 4 * (j + i));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(r[i], r[i + 1], 16);
+    }
+    __device__ __forceinline__ uint32_t dbits() const {
+        return *reinterpret_cast<const uint32_t *>(a + 208) >> 16;
+    }
+};
 
 // Row-group geometry of a CTA: rows [ra, ra + n) split into ng groups.
 struct Groups {
@@ -166,6 +164,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     kq_set_stream(const __grid_constant__ StreamParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int abort_flag;
+    __shared__ int gcount[2];  // warps done with the row group of each buffer
 
     int mi = 0;
 #pragma unroll 1
@@ -193,12 +192,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     float *part_f = reinterpret_cast<float *>(smem + 1024 + p.x_bytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t xbar = bars + 8 * (2 * kMaxSlots);  // inputs staged in shared memory
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < nslot; ++s) {
             mbar_init(bars + 8 * s, 1);
             mbar_init(bars + 8 * (kMaxSlots + s), kStreamConsumers);
         }
+        mbar_init(xbar, 1);
+        mbar_init(xbar + 8, 1);   // group reduction done, buffer 0
+        mbar_init(xbar + 16, 1);  // group reduction done, buffer 1
+        mbar_init(xbar + 24, kStreamConsumers);  // raw inputs consumed
+        gcount[0] = gcount[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -206,19 +211,37 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (warp == kStreamConsumers) {
         // ------------------------------------------------ producer
         if (lane != 0) return;
+        // The raw inputs go first, into the last ring slot, which is not
+        // filled with weights until the consumers have built their padded,
+        // scaled copy of them.
+        const uint32_t xraw = ring + (uint32_t)(nslot - 1) * p.slot_bytes;
+        if (XSMEM) {
+            const uint32_t xb = (uint32_t)(NTOK * (int64_t)nb * 256 * 4);
+            mbar_expect_tx(xbar, xb);
+            for (uint32_t o = 0; o < xb; o += 32768)
+                bulk_g2s(xraw + o, reinterpret_cast<const uint8_t *>(M.x) + o,
+                         xb - o < 32768 ? xb - o : 32768, xbar);
+        }
         int issued = 0;
+        int slot = 0, lap = 0, g = 0, k = 0;
+        int64_t g0 = G.start(0), g1 = G.start(1);
         for (int s = 0; s < nstage; ++s) {
-            const int slot = s % nslot;
-            if (s >= nslot) {
+            if (XSMEM && s == nslot - 1) {
                 if (*(volatile int *)&abort_flag) break;
-                if (!mbar_wait(bars + 8 * (kMaxSlots + slot), ((s / nslot) - 1) & 1)) {
+                if (!mbar_wait(xbar + 24, 0)) {
                     atomicExch(&abort_flag, 1);
                     atomicOr(p.err, 1u);
                     break;
                 }
             }
-            const int g = s / nbox, k = s - (s / nbox) * nbox;
-            const int64_t g0 = G.start(g), g1 = G.start(g + 1);
+            if (s >= nslot) {
+                if (*(volatile int *)&abort_flag) break;
+                if (!mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1)) {
+                    atomicExch(&abort_flag, 1);
+                    atomicOr(p.err, 1u);
+                    break;
+                }
+            }
             const int h = (int)(g1 - g0);
             const uint32_t dst = ring + (uint32_t)slot * p.slot_bytes;
             const uint32_t full = bars + 8 * slot;
@@ -245,9 +268,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 }
             }
             issued = s + 1;
+            if (++slot == nslot) {
+                slot = 0;
+                ++lap;
+            }
+            if (++k == nbox) {
+                k = 0;
+                ++g;
+                g0 = g1;
+                g1 = G.start(g + 1);
+            }
         }
         if (*(volatile int *)&abort_flag) {
             // do not leave copies in flight into this CTA's shared memory
+            if (XSMEM) mbar_wait(xbar, 0);
             for (int slot = 0; slot < nslot && slot < issued; ++slot) {
                 const int last = slot + ((issued - 1 - slot) / nslot) * nslot;
                 mbar_wait(bars + 8 * slot, (last / nslot) & 1);
@@ -258,28 +292,89 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     // ---------------------------------------------------- consumers
     const int64_t cols = (int64_t)nb * 256;
+    const bool q4 = fmt == kFmtQ4K;
+    // scaled inputs, padded to 260 floats a block so that the inputs of
+    // neighbouring block columns fall on different shared-memory banks
+    const int xstride = nb * 260;
+    const float *xs_f = reinterpret_cast<const float *>(smem + 1024);
+    const float *xt_f = xs_f + NTOK * xstride;  // sub-block sums
     if (XSMEM) {
-        const float4 *src = reinterpret_cast<const float4 *>(M.x);
-        float4 *dstx = reinterpret_cast<float4 *>(smem + 1024);
+        // The producer copies x into the last ring slot first.  Take the
+        // sub-block sums X_s from it (element order, as sum32 does from
+        // global memory), and write the copy scaled for the bit position of
+        // each weight's code (kq_blocks.cuh) into the padded layout.
+        if (!mbar_wait(xbar, 0)) {
+            atomicExch(&abort_flag, 1);
+            atomicOr(p.err, 1u);
+        }
+        const float *xr = reinterpret_cast<const float *>(
+            smem + (ring + (uint32_t)(nslot - 1) * p.slot_bytes - bars));
+        float *xw = reinterpret_cast<float *>(smem + 1024);
+        if (!q6) {
+            float *tab = xw + NTOK * xstride;
+            const int ns = (int)(NTOK * cols / 32);
+            for (int i = threadIdx.x; i < ns; i += kStreamConsumers * 32) {
+                const float4 *v4 = reinterpret_cast<const float4 *>(xr + 32 * i);
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 v = v4[j];
+                    acc += v.x;
+                    acc += v.y;
+                    acc += v.z;
+                    acc += v.w;
+                }
+                tab[i] = acc;
+            }
+        }
         const int n4 = (int)(NTOK * cols / 4);
-        for (int i = threadIdx.x; i < n4; i += kStreamConsumers * 32) dstx[i] = __ldg(src + i);
+        for (int i = threadIdx.x; i < n4; i += kStreamConsumers * 32) {
+            const int e = (4 * i) & 255;  // cols is a multiple of 256
+            const int blk = (4 * i) >> 8;  // token-major block index
+            float4 v = reinterpret_cast<const float4 *>(xr)[i];
+            v.x *= pow2f(xscale_exp(q4, e));
+            v.y *= pow2f(xscale_exp(q4, e + 1));
+            v.z *= pow2f(xscale_exp(q4, e + 2));
+            v.w *= pow2f(xscale_exp(q4, e + 3));
+            *reinterpret_cast<float4 *>(xw + blk * 260 + e) = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar + 24);  // the raw copy may be overwritten
     }
     consumer_sync();
 
+    // Row groups alternate between two partial buffers.  Each consumer warp
+    // counts itself done with a group after the group's last stage; the last
+    // warp to do so sums the group's partials in block order and writes y,
+    // then releases the buffer (mbarrier) for the group two later.  No
+    // consumer waits for the others at a group boundary.
+    const int part_floats = p.part_bytes / 8;  // per buffer
+    // A Q4_K / Q5_K task is one block column of two rows of the stage, p
+    // and p + hp, which share their inputs; a Q6_K task is one row.
+    const int rr = q6 ? 1 : 2;
     int batch_base = 0;
+    int slot = 0, lap = 0, g = 0, k = 0;
+    int64_t g0 = G.start(0), g1 = G.start(1);
+    int h = (int)(g1 - g0);
+    int hp = (h + rr - 1) / rr;
+    uint32_t hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
 #pragma unroll 1
     for (int s = 0; s < nstage; ++s) {
-        const int slot = s % nslot;
-        const int g = s / nbox, k = s - (s / nbox) * nbox;
-        const int64_t g0 = G.start(g), g1 = G.start(g + 1);
-        const int h = (int)(g1 - g0);
         const int b0 = q6 ? 0 : k * M.kb;
         const int kbv = q6 ? nb : (nb - b0 < M.kb ? nb - b0 : M.kb);
-        const int tasks = h * kbv;
+        const int tasks = hp * kbv;
         const int nbat = (tasks + 31) / 32;
         const uint32_t sdata = ring + (uint32_t)slot * p.slot_bytes;
+        const uint8_t *sdp = smem + (sdata - bars);
+        float *pbuf = part_f + (g & 1) * part_floats;
         bool ok = !*(volatile int *)&abort_flag;
-        if (ok && !mbar_wait(bars + 8 * slot, (s / nslot) & 1)) {
+        if (ok && k == 0 && g >= 2 &&
+            !mbar_wait(xbar + 8 + 8 * (g & 1), ((g >> 1) - 1) & 1)) {
+            atomicExch(&abort_flag, 1);
+            atomicOr(p.err, 1u);
+            ok = false;
+        }
+        if (ok && !mbar_wait(bars + 8 * slot, lap & 1)) {
             atomicExch(&abort_flag, 1);
             atomicOr(p.err, 1u);
             ok = false;
@@ -293,51 +388,55 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             for (; bat < batch_base + nbat; bat += kStreamConsumers) {
                 const int t = (bat - batch_base) * 32 + lane;
                 if (t >= tasks) continue;
-                const int j = t / h, r = t - (t / h) * h;
+                // t / hp by multiply-shift: exact for t < 2^11, hp <= 32
+                const int j = (int)(((uint32_t)t * hinv) >> 20), r = t - j * hp;
                 const int b = b0 + j;
-                float part[NTOK];
-                if (XSMEM) {
-                    const XShared xa{xs + (uint32_t)(b * 1024), (uint32_t)(cols * 4)};
+                const float *xsb = xs_f + b * 260;
+                const float *xtb = xt_f + b * 8;
+                const int xpl = xstride, spl = (int)(cols / 32);
+                if (!q6) {
+                    const int r2 = r + hp < h ? r + hp : h - 1;  // h odd: recompute, not stored
+                    const int bb45 = fmt == kFmtQ4K ? 144 : 176;
+                    const BlockShared B[2] = {
+                        {reinterpret_cast<const uint4 *>(sdp + r * M.kb * bb45 + j * bb45)},
+                        {reinterpret_cast<const uint4 *>(sdp + r2 * M.kb * bb45 + j * bb45)}};
+                    float part[2][NTOK];
                     if (fmt == kFmtQ4K) {
-                        uint4 v[9];
-                        const uint32_t a = sdata + (uint32_t)(r * M.kb * 144 + j * 144);
-#pragma unroll
-                        for (int i = 0; i < 9; ++i) v[i] = lds_v4(a + 16 * i);
-                        block_q45<NTOK, false>(v, xa, part);
-                    } else if (fmt == kFmtQ5K) {
-                        uint4 v[11];
-                        const uint32_t a = sdata + (uint32_t)(r * M.kb * 176 + j * 176);
-#pragma unroll
-                        for (int i = 0; i < 11; ++i) v[i] = lds_v4(a + 16 * i);
-                        block_q45<NTOK, true>(v, xa, part);
+                        if (XSMEM)
+                            block_q45<NTOK, false, 2>(B, XSharedS{xsb, xpl, xtb, spl}, part);
+                        else
+                            block_q45<NTOK, false, 2>(B, XGlobalS<true>{M.x + (int64_t)b * 256, cols}, part);
                     } else {
-                        uint32_t L[52], dbits;
-                        lds_q6(sdata + q6off + (uint32_t)((r * nb + j) * 210), L, dbits);
-                        block_q6<NTOK>(L, dbits, xa, part);
+                        if (XSMEM)
+                            block_q45<NTOK, true, 2>(B, XSharedS{xsb, xpl, xtb, spl}, part);
+                        else
+                            block_q45<NTOK, true, 2>(B, XGlobalS<false>{M.x + (int64_t)b * 256, cols}, part);
+                    }
+#pragma unroll
+                    for (int tt = 0; tt < NTOK; ++tt) {
+                        pbuf[((size_t)r * nb + b) * NTOK + tt] = part[0][tt];
+                        if (r + hp < h) pbuf[((size_t)r2 * nb + b) * NTOK + tt] = part[1][tt];
                     }
                 } else {
-                    const XGlobal xa{M.x + (int64_t)b * 256, cols};
-                    if (fmt == kFmtQ4K) {
-                        uint4 v[9];
-                        const uint32_t a = sdata + (uint32_t)(r * M.kb * 144 + j * 144);
-#pragma unroll
-                        for (int i = 0; i < 9; ++i) v[i] = lds_v4(a + 16 * i);
-                        block_q45<NTOK, false>(v, xa, part);
-                    } else if (fmt == kFmtQ5K) {
-                        uint4 v[11];
-                        const uint32_t a = sdata + (uint32_t)(r * M.kb * 176 + j * 176);
-#pragma unroll
-                        for (int i = 0; i < 11; ++i) v[i] = lds_v4(a + 16 * i);
-                        block_q45<NTOK, true>(v, xa, part);
+                    float part[NTOK];
+                    const uint8_t *a = sdp + q6off + (r * nb + j) * 210;
+                    const bool shifted = (smem_addr(a) & 3u) != 0;
+                    if (XSMEM) {
+                        const XSharedS xa{xsb, xpl, xtb, spl};
+                        if (shifted)
+                            block_q6k<NTOK>(Q6SharedShifted{a - 2}, xa, part);
+                        else
+                            block_q6k<NTOK>(Q6SharedAligned{a}, xa, part);
                     } else {
-                        uint32_t L[52], dbits;
-                        lds_q6(sdata + q6off + (uint32_t)((r * nb + j) * 210), L, dbits);
-                        block_q6<NTOK>(L, dbits, xa, part);
+                        const XGlobalS<false> xa{M.x + (int64_t)b * 256, cols};
+                        if (shifted)
+                            block_q6k<NTOK>(Q6SharedShifted{a - 2}, xa, part);
+                        else
+                            block_q6k<NTOK>(Q6SharedAligned{a}, xa, part);
                     }
-                }
 #pragma unroll
-                for (int tt = 0; tt < NTOK; ++tt)
-                    part_f[((size_t)r * nb + b) * NTOK + tt] = part[tt];
+                    for (int tt = 0; tt < NTOK; ++tt) pbuf[((size_t)r * nb + b) * NTOK + tt] = part[tt];
+                }
             }
         }
         batch_base += nbat;
@@ -345,17 +444,45 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (lane == 0) mbar_arrive(bars + 8 * (kMaxSlots + slot));
 
         if (k == nbox - 1) {
-            consumer_sync();  // every partial of group g is in shared memory
-            const bool bad = *(volatile int *)&abort_flag;
-#pragma unroll 1
-            for (int o = threadIdx.x; o < h * NTOK; o += kStreamConsumers * 32) {
-                const int r = o / NTOK, tt = o - (o / NTOK) * NTOK;
-                float acc = part_f[((size_t)r * nb) * NTOK + tt];
-#pragma unroll 1
-                for (int b = 1; b < nb; ++b) acc += part_f[((size_t)r * nb + b) * NTOK + tt];
-                M.y[(int64_t)tt * M.rows + g0 + r] = bad ? __int_as_float(0x7FC00000) : acc;
+            // this warp is done with group g
+            int old = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                old = atomicAdd(&gcount[g & 1], 1);
             }
-            consumer_sync();  // partials may be overwritten by the next group
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == kStreamConsumers - 1) {
+                __threadfence_block();
+                const bool bad = *(volatile int *)&abort_flag;
+                if (lane < h) {
+#pragma unroll 1
+                    for (int tt = 0; tt < NTOK; ++tt) {
+                        float acc = pbuf[((size_t)lane * nb) * NTOK + tt];
+#pragma unroll 4
+                        for (int b = 1; b < nb; ++b) acc += pbuf[((size_t)lane * nb + b) * NTOK + tt];
+                        M.y[(int64_t)tt * M.rows + g0 + lane] = bad ? __int_as_float(0x7FC00000) : acc;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    gcount[g & 1] = 0;
+                    __threadfence_block();
+                    mbar_arrive(xbar + 8 + 8 * (g & 1));
+                }
+            }
+        }
+        if (++slot == nslot) {
+            slot = 0;
+            ++lap;
+        }
+        if (++k == nbox) {
+            k = 0;
+            ++g;
+            g0 = g1;
+            g1 = G.start(g + 1);
+            h = (int)(g1 - g0);
+            hp = (h + rr - 1) / rr;
+            hinv = hp > 0 ? ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp : 1u;
         }
     }
 }

@@ -1,0 +1,85 @@
+// kq_launch.cuh -- kernel launch entry points, one set per token count.
+// Each kq_inst_<n>.cu instantiates them for ntok = n so that the kernels
+// compile in parallel translation units; kq_api.cu calls them through
+// kq_launch_direct / kq_launch_stream.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "kq_kernel_direct.cuh"
+#include "kq_kernel_stream.cuh"
+
+namespace kqlaunch {
+
+constexpr int kDirectSmemLimit = 200 * 1024;
+
+template <int NTOK>
+cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
+                          cudaStream_t stream) {
+    static std::mutex mu;
+    static size_t configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (smem > 48 * 1024) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev] < smem) {
+            e = cudaFuncSetAttribute(kq::kq_set_direct<NTOK>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kDirectSmemLimit);
+            if (e != cudaSuccess) return e;
+            configured[dev] = kDirectSmemLimit;
+        }
+    }
+    kq::kq_set_direct<NTOK><<<grid, kq::kDirectThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int NTOK, bool XSMEM>
+cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cudaStream_t s) {
+    static std::mutex mu;
+    static size_t configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev] < smem) {
+            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = smem;
+        }
+    }
+    kq::kq_set_stream<NTOK, XSMEM><<<grid, kq::kStreamThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ntok-dispatching entry points (defined in kq_api.cu from the instances)
+cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
+                   cudaStream_t s);
+
+}  // namespace kqlaunch
+
+#define KQ_DECLARE_INSTANCES(N)                                                            \
+    namespace kqlaunch {                                                                   \
+    extern template cudaError_t launch_direct<N>(const kq::SetParams &, int, size_t,       \
+                                                 cudaStream_t);                            \
+    extern template cudaError_t launch_stream<N, true>(const kq::StreamParams &, int,      \
+                                                       size_t, cudaStream_t);              \
+    extern template cudaError_t launch_stream<N, false>(const kq::StreamParams &, int,     \
+                                                        size_t, cudaStream_t);             \
+    }
+#define KQ_DEFINE_INSTANCES(N)                                                             \
+    namespace kqlaunch {                                                                   \
+    template cudaError_t launch_direct<N>(const kq::SetParams &, int, size_t, cudaStream_t); \
+    template cudaError_t launch_stream<N, true>(const kq::StreamParams &, int, size_t,     \
+                                                cudaStream_t);                             \
+    template cudaError_t launch_stream<N, false>(const kq::StreamParams &, int, size_t,    \
+                                                 cudaStream_t);                            \
+    }
