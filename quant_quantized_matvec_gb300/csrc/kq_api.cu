@@ -63,6 +63,25 @@ cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, si
 // Device error word: set by a kernel whose bounded wait expired.
 __device__ unsigned int g_kq_device_error;
 
+namespace kq {
+// Input records of every member, written to global memory (kq_xrec.cuh).
+__global__ void __launch_bounds__(kPrepThreads) kq_xprep(const __grid_constant__ PrepParams p) {
+    const int64_t w = ((int64_t)blockIdx.x * kPrepThreads + threadIdx.x) >> 5;
+    if (w >= p.first_warp[p.n]) return;
+    int mi = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.n; ++i)
+        if (w >= p.first_warp[i]) mi = i;
+    const int i = (int)(w - p.first_warp[mi]);
+    const int nb = p.nb[mi];
+    const bool q6 = p.q6[mi] != 0;
+    const int lane = threadIdx.x & 31;
+    const float4 v = record_inputs(p.x[mi], (int64_t)nb * 256, nb, i, lane);
+    build_record_half(v, p.rec[mi] + (int64_t)(i >> 1) * rec_bytes(q6), i & 1, q6, lane);
+}
+
+}  // namespace kq
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -160,6 +179,49 @@ cudaError_t device_info(int dev, DeviceInfo &out) {
 
 constexpr int kSmemLimit = kqlaunch::kDirectSmemLimit;
 
+// Input records of each member in global memory, for the kernels that do
+// not build them in shared memory: one stream-ordered allocation, written
+// by kq_xprep and released (in stream order) after the kernel that reads
+// them.
+struct GlobalRecords {
+    uint8_t *buf = nullptr;
+    const uint8_t *rec[KQ_MAX_SET] = {};
+};
+
+cudaError_t prepare_records(const kq_mat *mats, int n, int ntok, cudaStream_t s,
+                            GlobalRecords &out) {
+    kq::PrepParams p{};
+    p.n = n;
+    p.ntok = ntok;
+    int64_t off[KQ_MAX_SET], total = 0, warps = 0;
+    for (int i = 0; i < n; ++i) {
+        const int nb = (int)(mats[i].cols / 256);
+        const bool q6 = mats[i].fmt == KQ_Q6_K;
+        off[i] = total;
+        total += ((int64_t)ntok * nb * kq::rec_bytes(q6) + 255) / 256 * 256;
+        p.x[i] = mats[i].x;
+        p.nb[i] = nb;
+        p.q6[i] = q6 ? 1 : 0;
+        p.first_warp[i] = warps;
+        warps += (int64_t)ntok * nb * 2;
+    }
+    p.first_warp[n] = warps;
+    cudaError_t e = cudaMallocAsync((void **)&out.buf, (size_t)total, s);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i) {
+        p.rec[i] = out.buf + off[i];
+        out.rec[i] = p.rec[i];
+    }
+    const int64_t blocks = (warps * 32 + kq::kPrepThreads - 1) / kq::kPrepThreads;
+    kq::kq_xprep<<<(unsigned)blocks, kq::kPrepThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaFreeAsync(out.buf, s);
+        out.buf = nullptr;
+    }
+    return e;
+}
+
 // Plan and launch the direct-load kernel (any shape).
 kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
                      const DeviceInfo &info) {
@@ -191,7 +253,14 @@ kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         smem = std::max<size_t>(smem, (size_t)(per_row * rpc));
         if (grid > 0x7FFFFFFF) return KQ_ERR_SHAPE;
     }
-    const cudaError_t e = kqlaunch::direct(ntok, p, (int)grid, smem, s);
+    GlobalRecords gr;
+    cudaError_t e = prepare_records(mats, n, ntok, s, gr);
+    if (e == cudaSuccess) {
+        for (int i = 0; i < n; ++i) p.m[i].rec = gr.rec[i];
+        e = kqlaunch::direct(ntok, p, (int)grid, smem, s);
+        const cudaError_t ef = cudaFreeAsync(gr.buf, s);
+        if (e == cudaSuccess) e = ef;
+    }
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
@@ -321,7 +390,20 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         --used;
     }
 
-    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0, raw_x = 0;
+    // Q4_K / Q5_K stages are [h rows][kb blocks] boxes; Q6_K stages are a
+    // few whole rows, as many as fit the slot size the other members need
+    // (or 64 KiB when every member is Q6_K).
+    int64_t slot45 = 0;
+    for (int i = 0; i < n; ++i) {
+        if (mats[i].fmt == KQ_Q6_K) continue;
+        const int nb = (int)(mats[i].cols / 256);
+        const int bb = (int)block_bytes_of(mats[i].fmt);
+        const int kbmax = (int)std::min<int64_t>(nb, 2048 / bb);
+        slot45 = std::max<int64_t>(slot45, 32 * (int64_t)kbmax * bb);
+    }
+    const int64_t q6_target = slot45 > 0 ? slot45 : 64 * 1024;
+
+    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0;
     int cta = 0;
     for (int i = 0; i < n; ++i) {
         const kq_mat &m = mats[i];
@@ -342,7 +424,8 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         const int64_t part_row = (int64_t)nb * ntok * 4;
         int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, 32);
         if (m.fmt == KQ_Q6_K)
-            rmax = (int)std::min<int64_t>(rmax, std::min<int64_t>(16, (65536 - 32) / row_bytes));
+            rmax = (int)std::min<int64_t>(
+                rmax, std::max<int64_t>(1, std::min<int64_t>(16, (q6_target - 32) / row_bytes)));
         if (rmax < 1) return KQ_ERR_SHAPE;
         M.rmax = rmax;
         // Blocks per box: a box row is at most 2048 bytes (256 u64); prefer
@@ -379,6 +462,16 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
                 hmax = std::max<int>(hmax, (int)hh);
             }
         }
+        // tasks of a stage (row pairs x block columns) stay below 2^12, the
+        // range of the kernel's multiply-shift division
+        {
+            int hp = hmax;
+            if (kq::stream_rows_per_task(m.fmt, ntok) == 2) {
+                hp = (hmax + 1) / 2;
+                if (m.fmt == KQ_Q6_K && (nb & 1) && (hp & 1) && hmax > 1) ++hp;
+            }
+            if ((int64_t)hp * (m.fmt == KQ_Q6_K ? nb : M.kb) >= 4096) return KQ_ERR_SHAPE;
+        }
         M.nmaps = m.fmt == KQ_Q6_K ? 0 : nh;
         if (m.fmt != KQ_Q6_K) {
             const int box_w = (int)(M.kb * bb / 8);
@@ -391,22 +484,19 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         } else {
             slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * row_bytes + 32);
         }
-        // scaled inputs [ntok][nb][260] (a 16-byte pad per block) and
-        // sub-block sums [ntok][cols/32]
-        x_bytes = std::max<int64_t>(
-            x_bytes, round_up((int64_t)ntok * nb * 260 * 4 + (int64_t)ntok * m.cols / 8, 128));
-        raw_x = std::max<int64_t>(raw_x, (int64_t)ntok * m.cols * 4);
+        // input records [ntok][nb] (kq_xrec.cuh)
+        x_bytes = std::max<int64_t>(x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
         part_bytes = std::max<int64_t>(part_bytes, (int64_t)hmax * part_row);
     }
-    const bool xsmem = x_bytes <= 72 * 1024;
-    if (!xsmem) x_bytes = 0;
-    // with inputs in shared memory the raw copy is staged in a ring slot
-    if (xsmem) slot_bytes = std::max(slot_bytes, raw_x);
     part_bytes = 2 * round_up(part_bytes, 128);  // two row groups in flight
     slot_bytes = round_up(slot_bytes, 128);
-    const int64_t fixed = 1024 + x_bytes + part_bytes;
+    x_bytes = round_up(x_bytes, 128);
     // the 1 KiB alignment of the dynamic region pads the static part to 1 KiB
     const int64_t budget = (int64_t)info.smem_optin - 1024;
+    // input records in shared memory when two slots still fit beside them
+    const bool xsmem = 1024 + x_bytes + part_bytes + 2 * slot_bytes <= budget;
+    if (!xsmem) x_bytes = 0;
+    const int64_t fixed = 1024 + x_bytes + part_bytes;
     const int64_t nslot = std::min<int64_t>(kq::kMaxSlots, (budget - fixed) / slot_bytes);
     if (nslot < 2) return KQ_ERR_SHAPE;
     p.nslot = (int)nslot;
@@ -415,8 +505,20 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.part_bytes = (int)part_bytes;
     p.err = info.err;
     const size_t smem = (size_t)(fixed + nslot * slot_bytes);
-    const cudaError_t e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s);
     *launched = true;
+    GlobalRecords gr;
+    cudaError_t e = cudaSuccess;
+    if (!xsmem) {
+        e = prepare_records(mats, n, ntok, s, gr);
+        for (int i = 0; i < n; ++i) p.m[i].rec = gr.rec[i];
+    }
+    if (e == cudaSuccess) {
+        e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s);
+        if (gr.buf) {
+            const cudaError_t ef = cudaFreeAsync(gr.buf, s);
+            if (e == cudaSuccess) e = ef;
+        }
+    }
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;

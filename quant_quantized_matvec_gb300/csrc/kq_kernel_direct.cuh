@@ -1,16 +1,18 @@
-// kq_kernel_direct.cuh -- the set kernel, direct-load variant.
+// kq_kernel_direct.cuh -- the set kernel, direct-load variant, and the pass
+// that writes the input records to global memory for it.
 //
 // One CTA owns `rpc` consecutive rows of one member of the set.  Its
 // (row, block) pairs are spread over the CTA's threads, block-column major,
 // so neighbouring lanes take neighbouring rows of the same block column and
-// read the same inputs.  Every thread loads its super-block straight from
-// global memory with 16-byte (Q4_K, Q5_K) or 4-byte (Q6_K, whose 210-byte
-// blocks are only 2-byte aligned) read-only loads, computes the block's
-// contribution to each token (kq_blocks.cuh; inputs are read from global
-// memory and scaled on the fly), and parks it in shared memory.
-// After one barrier each (row, token) sums its blocks in block order 0..nb-1
-// and writes y.  The sum order depends on nothing but nb, so a member's
-// output is the same whichever set, grid or row split it runs in.
+// read the same input record.  Every thread loads its super-block straight
+// from global memory with 16-byte (Q4_K, Q5_K) or 4-byte (Q6_K, whose
+// 210-byte blocks are only 2-byte aligned) read-only loads, computes the
+// block's contribution to each token (kq_blocks.cuh, one row at a time)
+// from the records in global memory, and parks it in shared memory.  After
+// one barrier each (row, token) sums its blocks in block order 0..nb-1 and
+// writes y.  The sum order depends on nothing but nb, so a member's output
+// is the same whichever set, grid or row split it runs in, and the same as
+// the streaming kernel's.
 #pragma once
 
 #include "kq_blocks.cuh"
@@ -18,6 +20,20 @@
 namespace kq {
 
 constexpr int kDirectThreads = 256;
+constexpr int kPrepThreads = 256;
+
+// Input records in global memory for each member (kq_xprep in kq_api.cu):
+// warp w of the grid builds one 128-input half (kq_xrec.cuh).  Members are
+// laid out one after another in warp order (first_warp).
+struct PrepParams {
+    const float *x[kMaxSet];
+    uint8_t *rec[kMaxSet];
+    int32_t nb[kMaxSet];
+    int32_t q6[kMaxSet];
+    int64_t first_warp[kMaxSet + 1];
+    int32_t n;
+    int32_t ntok;
+};
 
 template <int NTOK>
 __global__ void __launch_bounds__(kDirectThreads)
@@ -32,7 +48,6 @@ __global__ void __launch_bounds__(kDirectThreads)
     const int64_t r0 = (int64_t)((int)blockIdx.x - M.cta_begin) * M.rpc;
     const int R = (int)min((int64_t)M.rpc, M.rows - r0);
     const int nb = M.nb;
-    const int64_t cols = (int64_t)nb * 256;
     const int tasks = R * nb;
 
 #pragma unroll 1
@@ -40,29 +55,29 @@ __global__ void __launch_bounds__(kDirectThreads)
         const int b = task / R;
         const int r = task - b * R;
         const int64_t blk_index = (r0 + r) * nb + b;
-        const float *xb = M.x + (int64_t)b * 256;
-        float part[NTOK];
-        if (M.fmt == kFmtQ4K) {
-            const BlockGlobal B[1] = {{reinterpret_cast<const uint4 *>(M.W + blk_index * 144)}};
-            float p1[1][NTOK];
-            block_q45<NTOK, false, 1>(B, XGlobalS<true>{xb, cols}, p1);
-#pragma unroll
-            for (int t = 0; t < NTOK; ++t) part[t] = p1[0][t];
-        } else if (M.fmt == kFmtQ5K) {
-            const BlockGlobal B[1] = {{reinterpret_cast<const uint4 *>(M.W + blk_index * 176)}};
-            float p1[1][NTOK];
-            block_q45<NTOK, true, 1>(B, XGlobalS<false>{xb, cols}, p1);
-#pragma unroll
-            for (int t = 0; t < NTOK; ++t) part[t] = p1[0][t];
-        } else {
+        float part[1][NTOK];
+        if (M.fmt == kFmtQ6K) {
+            const Rec<true> xr{M.rec + (int64_t)b * kRecQ6, nb * kRecQ6};
             const uint8_t *a = M.W + blk_index * 210;
-            if ((uintptr_t)a & 3u)
-                block_q6k<NTOK>(Q6GlobalShifted{a - 2}, XGlobalS<false>{xb, cols}, part);
-            else
-                block_q6k<NTOK>(Q6GlobalAligned{a}, XGlobalS<false>{xb, cols}, part);
+            if ((uintptr_t)a & 3u) {
+                const Q6Words<true, true> W[1] = {{a - 2}};
+                block_q6k<NTOK, 1>(W, xr, part);
+            } else {
+                const Q6Words<false, true> W[1] = {{a}};
+                block_q6k<NTOK, 1>(W, xr, part);
+            }
+        } else {
+            const Rec<true> xr{M.rec + (int64_t)b * kRecQ45, nb * kRecQ45};
+            if (M.fmt == kFmtQ4K) {
+                const BlockGlobal B[1] = {{reinterpret_cast<const uint4 *>(M.W + blk_index * 144)}};
+                block_q45<NTOK, false, 1>(B, xr, part);
+            } else {
+                const BlockGlobal B[1] = {{reinterpret_cast<const uint4 *>(M.W + blk_index * 176)}};
+                block_q45<NTOK, true, 1>(B, xr, part);
+            }
         }
 #pragma unroll
-        for (int t = 0; t < NTOK; ++t) part_s[(b * R + r) * NTOK + t] = part[t];
+        for (int t = 0; t < NTOK; ++t) part_s[(b * R + r) * NTOK + t] = part[0][t];
     }
     __syncthreads();
 

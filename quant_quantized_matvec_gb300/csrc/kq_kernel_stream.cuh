@@ -2,21 +2,25 @@
 //
 // One CTA per SM.  Each CTA owns a balanced, contiguous row range of one
 // member of the set, split into row groups of at most 32 rows (Q4_K, Q5_K)
-// or 16 rows (Q6_K).  A producer warp streams the weights through a ring of
-// shared-memory slots:
+// or a few rows (Q6_K, whose rows are long).  A producer warp streams the
+// weights through a ring of shared-memory slots:
 //   * Q4_K / Q5_K: one 2-D tensor-map box per stage, [h rows][kb blocks]
-//     (kb = 7: 1008 B / 1232 B per row, an odd number of 16-byte units, so
+//     (kb chosen so that a box row is an odd number of 16-byte units and
 //     rows land on distinct shared-memory banks), cp.async.bulk.tensor;
 //   * Q6_K: the group's whole rows, which are contiguous in memory but only
 //     2-byte aligned, as 16-byte-aligned bulk copies (cp.async.bulk) of at
 //     most 32 KiB, the sub-16-byte tail at the end of the matrix copied by
 //     the producer with plain loads.
-// Every consumer warp takes part in every stage: the stage's (row, block)
-// pairs, ordered block-major so neighbouring lanes share inputs, are dealt
-// out 32 at a time round-robin over the consumer warps, and each lane turns
-// one super-block into per-token partial sums (kq_blocks.cuh) stored in
-// shared memory.  When a row group's last stage is done the consumers sum
-// each row's blocks in block order 0..nb-1 and write y.  That sum order, and
+// Meanwhile the consumer warps turn the inputs into the fixed-point records
+// of kq_xrec.cuh in shared memory (or read them from global memory, where a
+// separate pass wrote them, when they do not fit).  Every consumer warp
+// takes part in every stage: the stage's tasks -- one block column of two
+// rows, p and p + hp, that share their inputs -- ordered block-major so
+// neighbouring lanes share inputs, are dealt out 32 at a time round-robin
+// over the consumer warps; each lane turns its two super-blocks into
+// per-token partial sums (kq_blocks.cuh) stored in shared memory.  When a
+// row group's last stage is done, the last warp to finish it sums each
+// row's blocks in block order 0..nb-1 and writes y.  That sum order, and
 // each block's arithmetic, depend only on the format, nb and ntok, so a
 // member's output is independent of the grid, the row split and the set.
 //
@@ -41,6 +45,7 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 struct StreamMember {
     const uint8_t *W;
     const float *x;
+    const uint8_t *rec;  // input records in global memory (when not staged)
     float *y;
     int64_t rows;
     int32_t nb;
@@ -59,7 +64,7 @@ struct StreamParams {
     int32_t n;
     int32_t nslot;
     int32_t slot_bytes;
-    int32_t x_bytes;     // 0: inputs are read from global memory
+    int32_t x_bytes;     // input records in shared memory (0: in global memory)
     int32_t part_bytes;
     unsigned int *err;   // device error word (nonzero: a wait expired)
 };
@@ -124,29 +129,26 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kStreamConsumers * 32) : "memory");
 }
 
-
-// Word sources for Q6_K blocks staged in shared memory (kq_blocks.cuh).
-struct Q6SharedAligned {
-    const uint8_t *a;
-    __device__ __forceinline__ void words4(int j, uint32_t (&o)[4]) const {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = *reinterpret_cast<const uint32_t *>(a + 4 * (j + i));
+// Words of a Q6_K block staged in shared memory, 2-byte aligned: five
+// aligned words funnel-shifted by 0 or 16 bits, the same instructions for
+// either alignment (a warp's lanes do not split over the two).  The word
+// after the block may be read (it lies inside the slot) and is discarded.
+struct Q6WordsShared {
+    const uint8_t *a4;  // block start rounded down to 4 bytes
+    uint32_t sh;        // 8 * (block start - a4)
+    static __device__ __forceinline__ Q6WordsShared at(const uint8_t *p) {
+        const uintptr_t u = reinterpret_cast<uintptr_t>(p);
+        return {reinterpret_cast<const uint8_t *>(u & ~(uintptr_t)3), (uint32_t)(u & 3u) * 8u};
     }
-    __device__ __forceinline__ uint32_t dbits() const {
-        return *reinterpret_cast<const uint16_t *>(a + 208);
-    }
-};
-struct Q6SharedShifted {  // a = block start - 2 (4-byte aligned)
-    const uint8_t *a;
     __device__ __forceinline__ void words4(int j, uint32_t (&o)[4]) const {
         uint32_t r[5];
 #pragma unroll
-        for (int i = 0; i < 5; ++i) r[i] = *reinterpret_cast<const uint32_t *>(a + 4 * (j + i));
+        for (int i = 0; i < 5; ++i) r[i] = reinterpret_cast<const uint32_t *>(a4)[j + i];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(r[i], r[i + 1], 16);
+        for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(r[i], r[i + 1], sh);
     }
     __device__ __forceinline__ uint32_t dbits() const {
-        return *reinterpret_cast<const uint32_t *>(a + 208) >> 16;
+        return *reinterpret_cast<const unsigned short *>(a4 + sh / 8 + 208);
     }
 };
 
@@ -159,12 +161,168 @@ struct Groups {
     }
 };
 
+// Row pairs of a stage of h rows: rows p and p + hp for p < hp.  Q6_K rows
+// p and p + hp must start with the same 4-byte alignment, which holds when
+// hp * nb is even.
+template <bool Q6>
+__device__ __forceinline__ int pair_offset(int h, int nb) {
+    int hp = (h + 1) >> 1;
+    if (Q6 && (nb & 1) && (hp & 1) && h > 1) ++hp;
+    return hp;
+}
+
+// Rows of one task: a lane takes one block column of R rows of the stage,
+// p and p + hp, which share their inputs.
+__host__ __device__ constexpr int stream_rows_per_task(int fmt, int ntok) {
+    return (void)fmt, (void)ntok, 2;
+}
+
+// What the consumer warps share.
+struct ConsumerCtx {
+    uint8_t *smem;
+    const uint8_t *recs;  // this member's input records (shared or global)
+    float *part_f;
+    int part_floats;      // floats per partial buffer
+    uint32_t bars, ring, xbar;
+    int nslot, slot_bytes;
+    int nb, kb, nbox, nstage;
+    int64_t rows, row_bytes;
+    float *y;
+    Groups G;
+    int *abort_flag;
+    int *gcount;
+    unsigned int *err;
+};
+
+template <int NTOK, bool XSMEM, int FMT>
+__device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane) {
+    constexpr bool Q6 = FMT == kFmtQ6K;
+    constexpr bool Q5 = FMT == kFmtQ5K;
+    constexpr int BB = Q6 ? 210 : (Q5 ? 176 : 144);
+    constexpr int REC = rec_bytes(Q6);
+    constexpr int R = stream_rows_per_task(FMT, NTOK);
+    using XR = Rec<!XSMEM>;
+    const int nb = c.nb;
+    const int tstride = nb * REC;
+    int batch_base = 0;
+    int slot = 0, lap = 0, g = 0, k = 0;
+    int64_t g0 = c.G.start(0), g1 = c.G.start(1);
+    int h = (int)(g1 - g0);
+    int hp = R == 2 ? pair_offset<Q6>(h, nb) : h;
+    uint32_t hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
+#pragma unroll 1
+    for (int s = 0; s < c.nstage; ++s) {
+        const int b0 = Q6 ? 0 : k * c.kb;
+        const int kbv = Q6 ? nb : (nb - b0 < c.kb ? nb - b0 : c.kb);
+        const int tasks = hp * kbv;
+        const int nbat = (tasks + 31) / 32;
+        const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
+        float *pbuf = c.part_f + (g & 1) * c.part_floats;
+        bool ok = !*(volatile int *)c.abort_flag;
+        if (ok && k == 0 && g >= 2 && !mbar_wait(c.xbar + 8 * (g & 1), ((g >> 1) - 1) & 1)) {
+            atomicExch(c.abort_flag, 1);
+            atomicOr(c.err, 1u);
+            ok = false;
+        }
+        if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1)) {
+            atomicExch(c.abort_flag, 1);
+            atomicOr(c.err, 1u);
+            ok = false;
+        }
+        if (ok) {
+            // byte offset of the group's first row inside the slot (Q6_K)
+            const uint32_t q6off = Q6 ? (uint32_t)((g0 * c.row_bytes) & 15) : 0u;
+            int bat = batch_base + ((warp - batch_base % kStreamConsumers) + kStreamConsumers) %
+                                       kStreamConsumers;
+#pragma unroll 1
+            for (; bat < batch_base + nbat; bat += kStreamConsumers) {
+                const int t = (bat - batch_base) * 32 + lane;
+                if (t >= tasks) continue;
+                // t / hp by multiply-shift: exact for t < 2^12, hp <= 32 (the
+                // planner keeps every stage below 2^12 tasks)
+                const int j = (int)(((uint32_t)t * hinv) >> 20), r = t - j * hp;
+                const int r2 = (R == 2 && r + hp < h) ? r + hp : r;
+                const int b = b0 + j;
+                const XR xr{c.recs + b * REC, tstride};
+                float part[R][NTOK];
+                if (!Q6) {
+                    BlockShared B[R];
+                    B[0].p = reinterpret_cast<const uint4 *>(sdp + (r * c.kb + j) * BB);
+                    if (R == 2) B[R - 1].p = reinterpret_cast<const uint4 *>(sdp + (r2 * c.kb + j) * BB);
+                    block_q45<NTOK, Q5, R>(B, xr, part);
+                } else {
+                    // both rows' blocks share one alignment; one code path
+                    // for every lane, whatever its block's alignment
+                    const uint8_t *a0 = sdp + q6off + (r * nb + j) * 210;
+                    const uint8_t *a1 = sdp + q6off + (r2 * nb + j) * 210;
+                    Q6WordsShared W[R];
+                    W[0] = Q6WordsShared::at(a0);
+                    if (R == 2) W[R - 1] = Q6WordsShared::at(a1);
+                    block_q6k<NTOK, R>(W, xr, part);
+                }
+#pragma unroll
+                for (int tt = 0; tt < NTOK; ++tt) {
+                    pbuf[(r * nb + b) * NTOK + tt] = part[0][tt];
+                    if (R == 2 && r2 != r) pbuf[(r2 * nb + b) * NTOK + tt] = part[R - 1][tt];
+                }
+            }
+        }
+        batch_base += nbat;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bars + 8 * (kMaxSlots + slot));
+
+        if (k == c.nbox - 1) {
+            // this warp is done with group g
+            int old = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                old = atomicAdd(&c.gcount[g & 1], 1);
+            }
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == kStreamConsumers - 1) {
+                __threadfence_block();
+                const bool bad = *(volatile int *)c.abort_flag;
+                if (lane < h) {
+#pragma unroll 1
+                    for (int tt = 0; tt < NTOK; ++tt) {
+                        float acc = pbuf[(lane * nb) * NTOK + tt];
+#pragma unroll 4
+                        for (int bb = 1; bb < nb; ++bb) acc += pbuf[(lane * nb + bb) * NTOK + tt];
+                        c.y[(int64_t)tt * c.rows + g0 + lane] =
+                            bad ? __int_as_float(0x7FC00000) : acc;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    c.gcount[g & 1] = 0;
+                    __threadfence_block();
+                    mbar_arrive(c.xbar + 8 * (g & 1));
+                }
+            }
+        }
+        if (++slot == c.nslot) {
+            slot = 0;
+            ++lap;
+        }
+        if (++k == c.nbox) {
+            k = 0;
+            ++g;
+            g0 = g1;
+            g1 = c.G.start(g + 1);
+            h = (int)(g1 - g0);
+            hp = h < 1 ? 1 : (R == 2 ? pair_offset<Q6>(h, nb) : h);
+            hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
+        }
+    }
+}
+
 template <int NTOK, bool XSMEM>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     kq_set_stream(const __grid_constant__ StreamParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int abort_flag;
     __shared__ int gcount[2];  // warps done with the row group of each buffer
+    __shared__ int xissued;    // consumer warps whose input loads have gone out
 
     int mi = 0;
 #pragma unroll 1
@@ -185,14 +343,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int nstage = G.ng * nbox;
     const int nslot = p.nslot;
 
-    const uint32_t bars = smem_addr(smem);  // full[0..nslot), empty[..]
-    const uint32_t xs = bars + 1024;
-    const uint32_t parts = xs + p.x_bytes;
+    const uint32_t bars = smem_addr(smem);  // full[0..kMaxSlots), empty[..]
+    const uint32_t recs = bars + 1024;
+    const uint32_t parts = recs + p.x_bytes;
     const uint32_t ring = parts + p.part_bytes;
-    float *part_f = reinterpret_cast<float *>(smem + 1024 + p.x_bytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t xbar = bars + 8 * (2 * kMaxSlots);  // inputs staged in shared memory
+    const uint32_t xbar = bars + 8 * (2 * kMaxSlots);  // row group reduced, buffers 0 / 1
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < nslot; ++s) {
@@ -200,10 +357,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             mbar_init(bars + 8 * (kMaxSlots + s), kStreamConsumers);
         }
         mbar_init(xbar, 1);
-        mbar_init(xbar + 8, 1);   // group reduction done, buffer 0
-        mbar_init(xbar + 16, 1);  // group reduction done, buffer 1
-        mbar_init(xbar + 24, kStreamConsumers);  // raw inputs consumed
+        mbar_init(xbar + 8, 1);
         gcount[0] = gcount[1] = 0;
+        xissued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -211,31 +367,25 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (warp == kStreamConsumers) {
         // ------------------------------------------------ producer
         if (lane != 0) return;
-        // The raw inputs go first, into the last ring slot, which is not
-        // filled with weights until the consumers have built their padded,
-        // scaled copy of them.
-        const uint32_t xraw = ring + (uint32_t)(nslot - 1) * p.slot_bytes;
+        // The consumers' input loads go out first, so that they are not
+        // queued behind the weight stream: wait until every consumer warp
+        // has issued them (a relaxed counter; the loads need not be done).
         if (XSMEM) {
-            const uint32_t xb = (uint32_t)(NTOK * (int64_t)nb * 256 * 4);
-            mbar_expect_tx(xbar, xb);
-            for (uint32_t o = 0; o < xb; o += 32768)
-                bulk_g2s(xraw + o, reinterpret_cast<const uint8_t *>(M.x) + o,
-                         xb - o < 32768 ? xb - o : 32768, xbar);
-        }
-        int issued = 0;
-        int slot = 0, lap = 0, g = 0, k = 0;
-        int64_t g0 = G.start(0), g1 = G.start(1);
-        for (int s = 0; s < nstage; ++s) {
-            if (XSMEM && s == nslot - 1) {
-                if (*(volatile int *)&abort_flag) break;
-                if (!mbar_wait(xbar + 24, 0)) {
+            const unsigned long long t0 = global_ns();
+            while (*(volatile int *)&xissued < kStreamConsumers) {
+                if (global_ns() - t0 > kWaitLimitNs) {
                     atomicExch(&abort_flag, 1);
                     atomicOr(p.err, 1u);
                     break;
                 }
             }
+        }
+        int issued = 0;
+        int slot = 0, lap = 0, g = 0, k = 0;
+        int64_t g0 = G.start(0), g1 = G.start(1);
+        for (int s = 0; s < nstage; ++s) {
+            if (*(volatile int *)&abort_flag) break;
             if (s >= nslot) {
-                if (*(volatile int *)&abort_flag) break;
                 if (!mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1)) {
                     atomicExch(&abort_flag, 1);
                     atomicOr(p.err, 1u);
@@ -281,7 +431,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
         if (*(volatile int *)&abort_flag) {
             // do not leave copies in flight into this CTA's shared memory
-            if (XSMEM) mbar_wait(xbar, 0);
             for (int slot = 0; slot < nslot && slot < issued; ++slot) {
                 const int last = slot + ((issued - 1 - slot) / nslot) * nslot;
                 mbar_wait(bars + 8 * slot, (last / nslot) & 1);
@@ -291,200 +440,42 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 
     // ---------------------------------------------------- consumers
-    const int64_t cols = (int64_t)nb * 256;
-    const bool q4 = fmt == kFmtQ4K;
-    // scaled inputs, padded to 260 floats a block so that the inputs of
-    // neighbouring block columns fall on different shared-memory banks
-    const int xstride = nb * 260;
-    const float *xs_f = reinterpret_cast<const float *>(smem + 1024);
-    const float *xt_f = xs_f + NTOK * xstride;  // sub-block sums
     if (XSMEM) {
-        // The producer copies x into the last ring slot first.  Take the
-        // sub-block sums X_s from it (element order, as sum32 does from
-        // global memory), and write the copy scaled for the bit position of
-        // each weight's code (kq_blocks.cuh) into the padded layout.
-        if (!mbar_wait(xbar, 0)) {
-            atomicExch(&abort_flag, 1);
-            atomicOr(p.err, 1u);
-        }
-        const float *xr = reinterpret_cast<const float *>(
-            smem + (ring + (uint32_t)(nslot - 1) * p.slot_bytes - bars));
-        float *xw = reinterpret_cast<float *>(smem + 1024);
-        if (!q6) {
-            float *tab = xw + NTOK * xstride;
-            const int ns = (int)(NTOK * cols / 32);
-            for (int i = threadIdx.x; i < ns; i += kStreamConsumers * 32) {
-                const float4 *v4 = reinterpret_cast<const float4 *>(xr + 32 * i);
-                float acc = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 v = v4[j];
-                    acc += v.x;
-                    acc += v.y;
-                    acc += v.z;
-                    acc += v.w;
-                }
-                tab[i] = acc;
-            }
-        }
-        const int n4 = (int)(NTOK * cols / 4);
-        for (int i = threadIdx.x; i < n4; i += kStreamConsumers * 32) {
-            const int e = (4 * i) & 255;  // cols is a multiple of 256
-            const int blk = (4 * i) >> 8;  // token-major block index
-            float4 v = reinterpret_cast<const float4 *>(xr)[i];
-            v.x *= pow2f(xscale_exp(q4, e));
-            v.y *= pow2f(xscale_exp(q4, e + 1));
-            v.z *= pow2f(xscale_exp(q4, e + 2));
-            v.w *= pow2f(xscale_exp(q4, e + 3));
-            *reinterpret_cast<float4 *>(xw + blk * 260 + e) = v;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xbar + 24);  // the raw copy may be overwritten
+        build_records(M.x, (int64_t)nb * 256, NTOK, nb, q6, smem + (recs - bars), warp,
+                      kStreamConsumers, lane, [&] {
+                          if (lane == 0)
+                              asm volatile("red.relaxed.cta.shared::cta.add.u32 [%0], 1;" ::"r"(
+                                  smem_addr(&xissued)));
+                      });
+        consumer_sync();
     }
-    consumer_sync();
-
-    // Row groups alternate between two partial buffers.  Each consumer warp
-    // counts itself done with a group after the group's last stage; the last
-    // warp to do so sums the group's partials in block order and writes y,
-    // then releases the buffer (mbarrier) for the group two later.  No
-    // consumer waits for the others at a group boundary.
-    const int part_floats = p.part_bytes / 8;  // per buffer
-    // A Q4_K / Q5_K task is one block column of two rows of the stage, p
-    // and p + hp, which share their inputs; a Q6_K task is one row.
-    const int rr = q6 ? 1 : 2;
-    int batch_base = 0;
-    int slot = 0, lap = 0, g = 0, k = 0;
-    int64_t g0 = G.start(0), g1 = G.start(1);
-    int h = (int)(g1 - g0);
-    int hp = (h + rr - 1) / rr;
-    uint32_t hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
-#pragma unroll 1
-    for (int s = 0; s < nstage; ++s) {
-        const int b0 = q6 ? 0 : k * M.kb;
-        const int kbv = q6 ? nb : (nb - b0 < M.kb ? nb - b0 : M.kb);
-        const int tasks = hp * kbv;
-        const int nbat = (tasks + 31) / 32;
-        const uint32_t sdata = ring + (uint32_t)slot * p.slot_bytes;
-        const uint8_t *sdp = smem + (sdata - bars);
-        float *pbuf = part_f + (g & 1) * part_floats;
-        bool ok = !*(volatile int *)&abort_flag;
-        if (ok && k == 0 && g >= 2 &&
-            !mbar_wait(xbar + 8 + 8 * (g & 1), ((g >> 1) - 1) & 1)) {
-            atomicExch(&abort_flag, 1);
-            atomicOr(p.err, 1u);
-            ok = false;
-        }
-        if (ok && !mbar_wait(bars + 8 * slot, lap & 1)) {
-            atomicExch(&abort_flag, 1);
-            atomicOr(p.err, 1u);
-            ok = false;
-        }
-        if (ok) {
-            // stage-local byte offset of row r, block j
-            const uint32_t q6off = q6 ? (uint32_t)((g0 * row_bytes) & 15) : 0u;
-            int bat = batch_base + ((warp - batch_base % kStreamConsumers) + kStreamConsumers) %
-                                       kStreamConsumers;
-#pragma unroll 1
-            for (; bat < batch_base + nbat; bat += kStreamConsumers) {
-                const int t = (bat - batch_base) * 32 + lane;
-                if (t >= tasks) continue;
-                // t / hp by multiply-shift: exact for t < 2^11, hp <= 32
-                const int j = (int)(((uint32_t)t * hinv) >> 20), r = t - j * hp;
-                const int b = b0 + j;
-                const float *xsb = xs_f + b * 260;
-                const float *xtb = xt_f + b * 8;
-                const int xpl = xstride, spl = (int)(cols / 32);
-                if (!q6) {
-                    const int r2 = r + hp < h ? r + hp : h - 1;  // h odd: recompute, not stored
-                    const int bb45 = fmt == kFmtQ4K ? 144 : 176;
-                    const BlockShared B[2] = {
-                        {reinterpret_cast<const uint4 *>(sdp + r * M.kb * bb45 + j * bb45)},
-                        {reinterpret_cast<const uint4 *>(sdp + r2 * M.kb * bb45 + j * bb45)}};
-                    float part[2][NTOK];
-                    if (fmt == kFmtQ4K) {
-                        if (XSMEM)
-                            block_q45<NTOK, false, 2>(B, XSharedS{xsb, xpl, xtb, spl}, part);
-                        else
-                            block_q45<NTOK, false, 2>(B, XGlobalS<true>{M.x + (int64_t)b * 256, cols}, part);
-                    } else {
-                        if (XSMEM)
-                            block_q45<NTOK, true, 2>(B, XSharedS{xsb, xpl, xtb, spl}, part);
-                        else
-                            block_q45<NTOK, true, 2>(B, XGlobalS<false>{M.x + (int64_t)b * 256, cols}, part);
-                    }
-#pragma unroll
-                    for (int tt = 0; tt < NTOK; ++tt) {
-                        pbuf[((size_t)r * nb + b) * NTOK + tt] = part[0][tt];
-                        if (r + hp < h) pbuf[((size_t)r2 * nb + b) * NTOK + tt] = part[1][tt];
-                    }
-                } else {
-                    float part[NTOK];
-                    const uint8_t *a = sdp + q6off + (r * nb + j) * 210;
-                    const bool shifted = (smem_addr(a) & 3u) != 0;
-                    if (XSMEM) {
-                        const XSharedS xa{xsb, xpl, xtb, spl};
-                        if (shifted)
-                            block_q6k<NTOK>(Q6SharedShifted{a - 2}, xa, part);
-                        else
-                            block_q6k<NTOK>(Q6SharedAligned{a}, xa, part);
-                    } else {
-                        const XGlobalS<false> xa{M.x + (int64_t)b * 256, cols};
-                        if (shifted)
-                            block_q6k<NTOK>(Q6SharedShifted{a - 2}, xa, part);
-                        else
-                            block_q6k<NTOK>(Q6SharedAligned{a}, xa, part);
-                    }
-#pragma unroll
-                    for (int tt = 0; tt < NTOK; ++tt) pbuf[((size_t)r * nb + b) * NTOK + tt] = part[tt];
-                }
-            }
-        }
-        batch_base += nbat;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (kMaxSlots + slot));
-
-        if (k == nbox - 1) {
-            // this warp is done with group g
-            int old = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                old = atomicAdd(&gcount[g & 1], 1);
-            }
-            old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old == kStreamConsumers - 1) {
-                __threadfence_block();
-                const bool bad = *(volatile int *)&abort_flag;
-                if (lane < h) {
-#pragma unroll 1
-                    for (int tt = 0; tt < NTOK; ++tt) {
-                        float acc = pbuf[((size_t)lane * nb) * NTOK + tt];
-#pragma unroll 4
-                        for (int b = 1; b < nb; ++b) acc += pbuf[((size_t)lane * nb + b) * NTOK + tt];
-                        M.y[(int64_t)tt * M.rows + g0 + lane] = bad ? __int_as_float(0x7FC00000) : acc;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    gcount[g & 1] = 0;
-                    __threadfence_block();
-                    mbar_arrive(xbar + 8 + 8 * (g & 1));
-                }
-            }
-        }
-        if (++slot == nslot) {
-            slot = 0;
-            ++lap;
-        }
-        if (++k == nbox) {
-            k = 0;
-            ++g;
-            g0 = g1;
-            g1 = G.start(g + 1);
-            h = (int)(g1 - g0);
-            hp = (h + rr - 1) / rr;
-            hinv = hp > 0 ? ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp : 1u;
-        }
-    }
+    ConsumerCtx c;
+    c.smem = smem;
+    c.recs = XSMEM ? smem + (recs - bars) : M.rec;
+    c.part_f = reinterpret_cast<float *>(smem + (parts - bars));
+    c.part_floats = p.part_bytes / 8;
+    c.bars = bars;
+    c.ring = ring;
+    c.xbar = xbar;
+    c.nslot = nslot;
+    c.slot_bytes = p.slot_bytes;
+    c.nb = nb;
+    c.kb = M.kb;
+    c.nbox = nbox;
+    c.nstage = nstage;
+    c.rows = M.rows;
+    c.row_bytes = row_bytes;
+    c.y = M.y;
+    c.G = G;
+    c.abort_flag = &abort_flag;
+    c.gcount = gcount;
+    c.err = p.err;
+    if (fmt == kFmtQ4K)
+        consume<NTOK, XSMEM, kFmtQ4K>(c, warp, lane);
+    else if (fmt == kFmtQ5K)
+        consume<NTOK, XSMEM, kFmtQ5K>(c, warp, lane);
+    else
+        consume<NTOK, XSMEM, kFmtQ6K>(c, warp, lane);
 }
 
 }  // namespace kq

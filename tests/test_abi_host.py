@@ -123,3 +123,14 @@ def test_set_rejects(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no fallback"):
         _binding.load(str(tmp_path / "libkq.so"))
+
+
+def test_stage_task_division_is_exact():
+    """The streaming kernel splits a stage task index t into (block column,
+    row pair) as t // hp by multiply-shift: (t * ceil(2^20 / hp)) >> 20 in
+    32-bit arithmetic.  The planner keeps t below 2^12 and hp at most 32;
+    over that whole range the shortcut must equal the true quotient."""
+    for hp in range(1, 33):
+        hinv = ((1 << 20) + hp - 1) // hp
+        for t in range(4096):
+            assert ((t * hinv) & 0xFFFFFFFF) >> 20 == t // hp, (hp, t)
