@@ -167,6 +167,19 @@ kq_status kq_device_error(int clear);
  */
 int kq_select_kernel(int which);
 
+/*
+ * Launch overlap (off by default).  When on, each streaming-kernel launch
+ * may begin while the kernel before it on the same stream is still running
+ * (programmatic dependent launch): its CTAs start streaming W into shared
+ * memory as soon as SMs free up, and wait for the preceding kernel to
+ * complete -- with its memory visible -- before they read x or write y.
+ * PRECONDITION while on: no W of a call is written by the kernel that
+ * immediately precedes the call on its stream (weights that stay constant,
+ * as in inference).  Results are unchanged.  Process-wide; returns the
+ * previous setting (0/1); an argument other than 0 or 1 only queries.
+ */
+int kq_set_overlap(int enable);
+
 /* Library ABI version: (major << 16) | minor. */
 int kq_version(void);
 

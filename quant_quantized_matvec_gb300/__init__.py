@@ -145,6 +145,14 @@ def select_kernel(which: str) -> str:
     return {v: k for k, v in KERNELS.items()}[prev]
 
 
+def set_overlap(enable: bool) -> bool:
+    """Let each streaming launch overlap the kernel before it on the stream
+    (weights prefetched early; x read and y written only after that kernel
+    completes).  Requires that the preceding kernel does not write the
+    weights.  Returns the previous setting."""
+    return bool(_lib().kq_set_overlap(1 if enable else 0))
+
+
 def device_error(clear: bool = True) -> bool:
     """True if a kernel on the current device reported an expired wait
     (synchronous read of the device error word)."""

@@ -18,7 +18,8 @@ STATUS = {
 }
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
-           "kq_device_error", "kq_select_kernel", "kq_version")
+           "kq_device_error", "kq_select_kernel", "kq_set_overlap",
+           "kq_version")
 
 
 class KqMat(ctypes.Structure):
@@ -72,6 +73,8 @@ def load(path: str | None = None):
         lib.kq_device_error.restype = i32
         lib.kq_select_kernel.argtypes = [i32]
         lib.kq_select_kernel.restype = i32
+        lib.kq_set_overlap.argtypes = [i32]
+        lib.kq_set_overlap.restype = i32
         lib.kq_version.argtypes = []
         lib.kq_version.restype = i32
         if path is None:

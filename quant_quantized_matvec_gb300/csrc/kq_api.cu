@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kPrepThreads) kq_xprep(const __grid_constant__
     const int nb = p.nb[mi];
     const bool q6 = p.q6[mi] != 0;
     const int lane = threadIdx.x & 31;
-    const float4 v = record_inputs(p.x[mi], (int64_t)nb * 256, nb, i, lane);
+    const int t = (i >> 1) / nb, ih = i - 2 * nb * t;  // token, half within the token
+    const float4 v = record_inputs(p.x[mi], (int64_t)nb * 256, t, ih, lane);
     build_record_half(v, p.rec[mi] + (int64_t)(i >> 1) * rec_bytes(q6), i & 1, q6, lane);
 }
 
@@ -343,6 +344,13 @@ bool tensor_map(const void *W, int64_t rows, int64_t row_bytes, int box_w, int b
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
+// Consumer cost per weight byte of Q6_K relative to Q4_K, in sixteenths
+// (measured: the Q6_K block loop spends more instructions per byte).
+constexpr int64_t kCostQ6 = 32;
+
+// Launch overlap with the preceding kernel (kq_set_overlap).
+std::atomic<int> g_overlap{0};
+
 // Plan the streaming kernel.  Returns KQ_OK after launching, or
 // KQ_ERR_SHAPE when the shapes cannot be staged (caller falls back).
 kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
@@ -355,11 +363,14 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.n = n;
     const int G = info.sms;
 
-    // CTAs per member in proportion to its bytes (at least one, at most one
-    // per row), largest remainder first.
+    // CTAs per member in proportion to its work (at least one, at most one
+    // per row), largest remainder first.  Work is bytes weighted by the
+    // format's consumer cost per byte relative to Q4_K (kCostQ6 / 16 for
+    // Q6_K, whose blocks take more instructions per byte).
     int64_t bytes[KQ_MAX_SET], total = 0;
     for (int i = 0; i < n; ++i) {
         bytes[i] = mats[i].rows * (mats[i].cols / 256) * block_bytes_of(mats[i].fmt);
+        if (mats[i].fmt == KQ_Q6_K) bytes[i] = bytes[i] * kCostQ6 / 16;
         total += bytes[i];
     }
     int ncta[KQ_MAX_SET];
@@ -419,6 +430,8 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         M.fmt = m.fmt;
         M.cta_begin = cta;
         M.ncta = ncta[i];
+        M.rows_q = (int32_t)(m.rows / ncta[i]);
+        M.rows_r = (int32_t)(m.rows % ncta[i]);
         cta += ncta[i];
         // rows per group: partials for the group must fit in 64 KiB
         const int64_t part_row = (int64_t)nb * ntok * 4;
@@ -503,6 +516,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.slot_bytes = (int)slot_bytes;
     p.x_bytes = (int)x_bytes;
     p.part_bytes = (int)part_bytes;
+    p.overlap = g_overlap.load() ? 1 : 0;
     p.err = info.err;
     const size_t smem = (size_t)(fixed + nslot * slot_bytes);
     *launched = true;
@@ -638,6 +652,12 @@ int kq_select_kernel(int which) {
     return prev;
 }
 
-int kq_version(void) { return (1 << 16) | 0; }
+int kq_set_overlap(int enable) {
+    const int prev = g_overlap.load();
+    if (enable == 0 || enable == 1) g_overlap.store(enable);
+    return prev;
+}
+
+int kq_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

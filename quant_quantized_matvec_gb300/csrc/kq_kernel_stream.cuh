@@ -52,6 +52,7 @@ struct StreamMember {
     int32_t fmt;
     int32_t cta_begin;
     int32_t ncta;
+    int32_t rows_q, rows_r;  // rows / ncta, rows % ncta
     int32_t rmax;   // rows per group at most
     int32_t kb;     // blocks per box (Q4_K / Q5_K)
     int32_t nmaps;  // tensor maps (box heights) for this member
@@ -66,6 +67,7 @@ struct StreamParams {
     int32_t slot_bytes;
     int32_t x_bytes;     // input records in shared memory (0: in global memory)
     int32_t part_bytes;
+    int32_t overlap;     // launched to overlap the preceding kernel
     unsigned int *err;   // device error word (nonzero: a wait expired)
 };
 
@@ -125,6 +127,14 @@ __device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap *ma
         "l"(map), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
+// Programmatic dependent launch: let the next kernel on the stream launch,
+// and wait for the preceding one (no-ops for an ordinary launch).
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kStreamConsumers * 32) : "memory");
 }
@@ -152,12 +162,23 @@ struct Q6WordsShared {
     }
 };
 
-// Row-group geometry of a CTA: rows [ra, ra + n) split into ng groups.
+// Row-group geometry of a CTA: rows [ra, ra + n) split into ng groups of
+// gq or gq + 1 rows (the first gr groups one more), without divisions in
+// the stage loop.
 struct Groups {
     int64_t ra;
-    int n, ng;
+    int n, ng, gq, gr;
     __device__ __forceinline__ int64_t start(int g) const {
-        return ra + (int64_t)g * n / ng;
+        return ra + (int64_t)(g * gq + (g < gr ? g : gr));
+    }
+    // CTA cidx of a member whose rows split into ncta CTAs of rows_q or
+    // rows_q + 1 rows (the first rows_r CTAs one more)
+    __device__ __forceinline__ void init(int cidx, int rows_q, int rows_r, int rmax) {
+        ra = (int64_t)cidx * rows_q + (cidx < rows_r ? cidx : rows_r);
+        n = rows_q + (cidx < rows_r ? 1 : 0);
+        ng = (n + rmax - 1) / rmax;
+        gq = n / ng;
+        gr = n - gq * ng;
     }
 };
 
@@ -236,8 +257,12 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                                        kStreamConsumers;
 #pragma unroll 1
             for (; bat < batch_base + nbat; bat += kStreamConsumers) {
-                const int t = (bat - batch_base) * 32 + lane;
-                if (t >= tasks) continue;
+                // Lanes past the stage's last task redo the last task and do
+                // not store it: the whole warp runs the block code together,
+                // which keeps its loops warp-uniform.
+                const int tl = (bat - batch_base) * 32 + lane;
+                const bool valid = tl < tasks;
+                const int t = valid ? tl : tasks - 1;
                 // t / hp by multiply-shift: exact for t < 2^12, hp <= 32 (the
                 // planner keeps every stage below 2^12 tasks)
                 const int j = (int)(((uint32_t)t * hinv) >> 20), r = t - j * hp;
@@ -260,10 +285,12 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                     if (R == 2) W[R - 1] = Q6WordsShared::at(a1);
                     block_q6k<NTOK, R>(W, xr, part);
                 }
+                if (valid) {
 #pragma unroll
-                for (int tt = 0; tt < NTOK; ++tt) {
-                    pbuf[(r * nb + b) * NTOK + tt] = part[0][tt];
-                    if (R == 2 && r2 != r) pbuf[(r2 * nb + b) * NTOK + tt] = part[R - 1][tt];
+                    for (int tt = 0; tt < NTOK; ++tt) {
+                        pbuf[(r * nb + b) * NTOK + tt] = part[0][tt];
+                        if (R == 2 && r2 != r) pbuf[(r2 * nb + b) * NTOK + tt] = part[R - 1][tt];
+                    }
                 }
             }
         }
@@ -310,8 +337,11 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             g0 = g1;
             g1 = c.G.start(g + 1);
             h = (int)(g1 - g0);
-            hp = h < 1 ? 1 : (R == 2 ? pair_offset<Q6>(h, nb) : h);
-            hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
+            const int hp_next = h < 1 ? 1 : (R == 2 ? pair_offset<Q6>(h, nb) : h);
+            if (hp_next != hp) {
+                hp = hp_next;
+                hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
+            }
         }
     }
 }
@@ -335,9 +365,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int64_t row_bytes = (int64_t)nb * bb;
     const int cidx = (int)blockIdx.x - M.cta_begin;
     Groups G;
-    G.ra = M.rows * cidx / M.ncta;
-    G.n = (int)(M.rows * (cidx + 1) / M.ncta - G.ra);
-    G.ng = (G.n + M.rmax - 1) / M.rmax;
+    G.init(cidx, M.rows_q, M.rows_r, M.rmax);
     const bool q6 = fmt == kFmtQ6K;
     const int nbox = q6 ? 1 : (nb + M.kb - 1) / M.kb;
     const int nstage = G.ng * nbox;
@@ -350,6 +378,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t xbar = bars + 8 * (2 * kMaxSlots);  // row group reduced, buffers 0 / 1
+    allow_dependents();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < nslot; ++s) {
@@ -367,10 +396,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (warp == kStreamConsumers) {
         // ------------------------------------------------ producer
         if (lane != 0) return;
-        // The consumers' input loads go out first, so that they are not
-        // queued behind the weight stream: wait until every consumer warp
-        // has issued them (a relaxed counter; the loads need not be done).
-        if (XSMEM) {
+        // The consumers' input loads go out with the first weight requests,
+        // not queued behind the weight stream: wait until every consumer
+        // warp is about to issue them (a relaxed counter).  Not when the
+        // launch overlaps the preceding kernel: then the weights stream
+        // while the consumers wait for that kernel.
+        if (XSMEM && !p.overlap) {
             const unsigned long long t0 = global_ns();
             while (*(volatile int *)&xissued < kStreamConsumers) {
                 if (global_ns() - t0 > kWaitLimitNs) {
@@ -440,6 +471,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 
     // ---------------------------------------------------- consumers
+    // x (or its records) and y belong to the stream order: with an
+    // overlapping launch, wait for the preceding kernel first.
+    wait_prerequisites();
     if (XSMEM) {
         build_records(M.x, (int64_t)nb * 256, NTOK, nb, q6, smem + (recs - bars), warp,
                       kStreamConsumers, lane, [&] {

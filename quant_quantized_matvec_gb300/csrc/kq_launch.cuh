@@ -55,8 +55,19 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
             configured[dev] = smem;
         }
     }
-    kq::kq_set_stream<NTOK, XSMEM><<<grid, kq::kStreamThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kq::kStreamThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (p.overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM>, p);
 }
 
 // ntok-dispatching entry points (defined in kq_api.cu from the instances)

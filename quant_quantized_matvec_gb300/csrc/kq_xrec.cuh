@@ -118,15 +118,12 @@ __device__ __forceinline__ void build_record_half(float4 v, uint8_t *rec, int h,
     }
 }
 
-// The four inputs lane `lane` converts for half i (= 2 * (t * nb + j) + h).
-__device__ __forceinline__ float4 record_inputs(const float *x, int64_t cols, int nb, int i,
+// The four inputs lane `lane` converts for half i (= 2 * j + h) of token t.
+__device__ __forceinline__ float4 record_inputs(const float *x, int64_t cols, int t, int i,
                                                 int lane) {
-    const int h = i & 1, tj = i >> 1;
-    const int t = tj / nb, j = tj - t * nb;
-    const float *q = x + t * cols + (int64_t)j * 256 + 128 * h + 4 * lane;
+    const float *q = x + t * cols + (int64_t)(i >> 1) * 256 + 128 * (i & 1) + 4 * lane;
     float4 v;
-    // volatile: stays ahead, in program order, of the caller's signal that
-    // the loads have gone out
+    // volatile: issued in program order after the caller's signal
     asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(q));
@@ -135,10 +132,10 @@ __device__ __forceinline__ float4 record_inputs(const float *x, int64_t cols, in
 
 // All records of one input plane set: ntok tokens x nb columns, records
 // token-major ([t][j]) at `recs`.  Work is dealt in warp-sized halves over
-// `nwarps` warps (`w` is this warp's index), kRecBatch halves a warp at a time:
-// all loads of a batch are issued before any conversion, and `issued()` is
-// called once, right after the first batch's loads, so that the caller can
-// let other memory traffic start behind them.
+// `nwarps` warps (`w` is this warp's index), kRecBatch halves a warp at a
+// time: all loads of a batch are issued before any conversion.  `issued()`
+// is called once, as the first batch's loads go out (they are issued right
+// after it), so that the caller can start other memory traffic with them.
 constexpr int kRecBatch = 8;
 
 template <class F>
@@ -146,24 +143,28 @@ __device__ __forceinline__ void build_records(const float *x, int64_t cols, int 
                                               bool q6, uint8_t *recs, int w, int nwarps,
                                               int lane, F issued) {
     const int rb = rec_bytes(q6);
-    const int n = ntok * nb * 2;
+    const int n = nb * 2;  // halves per token
     bool first = true;
 #pragma unroll 1
-    for (int base = w; base < n || first; base += kRecBatch * nwarps) {
-        float4 v[kRecBatch];
+    for (int t = 0; t < ntok; ++t) {
+        uint8_t *rt = recs + (int64_t)t * nb * rb;
+#pragma unroll 1
+        for (int base = w; base < n || first; base += kRecBatch * nwarps) {
+            if (first) {
+                issued();
+                first = false;
+            }
+            float4 v[kRecBatch];
 #pragma unroll
-        for (int k = 0; k < kRecBatch; ++k) {
-            const int i = base + k * nwarps;
-            if (i < n) v[k] = record_inputs(x, cols, nb, i, lane);
-        }
-        if (first) {
-            issued();
-            first = false;
-        }
+            for (int k = 0; k < kRecBatch; ++k) {
+                const int i = base + k * nwarps;
+                if (i < n) v[k] = record_inputs(x, cols, t, i, lane);
+            }
 #pragma unroll
-        for (int k = 0; k < kRecBatch; ++k) {
-            const int i = base + k * nwarps;
-            if (i < n) build_record_half(v[k], recs + (int64_t)(i >> 1) * rb, i & 1, q6, lane);
+            for (int k = 0; k < kRecBatch; ++k) {
+                const int i = base + k * nwarps;
+                if (i < n) build_record_half(v[k], rt + (i >> 1) * rb, i & 1, q6, lane);
+            }
         }
     }
 }

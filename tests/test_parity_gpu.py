@@ -109,3 +109,37 @@ def test_stream_equals_direct(fmt, ntok, rows, cols):
     assert np.array_equal(outs["direct"].view(np.uint32),
                           outs["stream"].view(np.uint32))
     C.check(fmt, W, rows, cols, x, outs["stream"], what="stream kernel")
+
+
+@pytest.mark.gpu
+def test_overlap_chain_equals_serial():
+    """With launch overlap on, each call streams its weights while the call
+    before it is still running but reads x only after that call completes.
+    A chain whose every input is the previous call's output must give the
+    same bits as with overlap off."""
+    cols = 1024
+    chain = [(kq.Q4_K, "c0"), (kq.Q6_K, "c1"), (kq.Q5_K, "c2"), (kq.Q4_K, "c3")]
+    Ws = [C.to_dev(C.case(f, cols, cols, 1, f"chain/{tag}")[0]) for f, tag in chain]
+    x0 = C.to_dev(C.case(kq.Q4_K, cols, cols, 1, "chain/x")[1])
+
+    def run():
+        ys = [torch.empty((1, cols), dtype=torch.float32, device="cuda") for _ in chain]
+        for rep in range(5):
+            x = x0
+            for (f, _), Wd, y in zip(chain, Ws, ys):
+                kq.matvec(f, Wd, cols, cols, x, y=y)
+                x = y
+        torch.cuda.synchronize()
+        return [y.cpu().numpy() for y in ys]
+
+    prev = kq.set_overlap(False)
+    try:
+        serial = run()
+        kq.set_overlap(True)
+        overlapped = run()
+    finally:
+        kq.set_overlap(prev)
+    assert not kq.device_error()
+    for a, b in zip(serial, overlapped):
+        assert np.isfinite(a).all()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
