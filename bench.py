@@ -15,7 +15,11 @@ bracketed by CUDA events on the launching stream with a barrier and a device
 synchronize on both sides; the weights rotate over enough copies that their
 total exceeds three times the L2 size, so every step streams from HBM.
 `value` = algorithmic bytes (weights + x once per distinct plane + y) of all
-steps on all ranks / max-over-ranks elapsed time.  `e2e` times the public
+steps on all ranks / max-over-ranks elapsed time.  By default the calls run
+with launch overlap on (kq_set_overlap: a call streams its weights while the
+previous call finishes and reads x only after that call completes); the
+same K steps with overlap off are timed too and reported as `serial`
+(--no-overlap makes them the headline).  `e2e` times the public
 Python API with the per-step input x copied from pinned host memory and the
 outputs copied back inside the timed region (weights stay resident, as model
 weights do).  `cpu_baseline` times the CPU oracle on a bounded sample.
@@ -259,56 +263,65 @@ def run_ours(args, rank, world, dist):
         mem, d = sets[i % len(sets)]
         kq.matvec_set(mem, ntok=ntok, stream=stream, descriptors=d)
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i)
-    torch.cuda.synchronize()
-
-    # CUDA graphs of L steps, replayed to make exactly K steps
     K = args.steps
     L = min(K, args.graph_len)
-    graphs = []
 
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
+    def timed(overlap, sampler=None):
+        """K steps replayed from CUDA graphs of L steps, captured with the
+        given launch-overlap setting; -> ms (max over ranks), wall s."""
+        kq.set_overlap(overlap)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
                 step(i)
-        return g
+        torch.cuda.synchronize()
 
-    g_main = capture(L)
-    reps, rem = K // L, K % L
-    g_rem = capture(rem) if rem else None
-    with torch.cuda.stream(stream):
-        g_main.replay()  # untimed warm replay of the graph itself
-    torch.cuda.synchronize()
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(i)
+            return g
 
+        g_main = capture(L)
+        reps, rem = K // L, K % L
+        g_rem = capture(rem) if rem else None
+        with torch.cuda.stream(stream):
+            g_main.replay()  # untimed warm replay of the graph itself
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+        if dist:
+            dist.barrier()
+        ms = ev0.elapsed_time(ev1)
+        if dist:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, wall, (reps, rem)
+
+    overlap = not args.no_overlap
+    ms_serial, _, _ = timed(False)
     sampler = ClockSampler(dev.index)
-    sampler.start()
-    time.sleep(0.3)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(reps):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t_wall
-    if dist:
-        dist.barrier()
+    ms, wall, (reps, rem) = timed(overlap, sampler)
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    kernels = kq.last_kernels()
+    launches_per_step = sum(kernels.values())
     total_bytes = step_bytes * K * world
     gbs = total_bytes / (ms * 1e-3) / 1e9
     us_per_step = ms * 1e3 / K
@@ -320,6 +333,7 @@ def run_ours(args, rank, world, dist):
     Ke = min(K, args.e2e_steps)
     h2d = sum(x.numel() * 4 for x in x_host.values())
     d2h = y_host.numel() * 4
+    kq.set_overlap(overlap)
     with torch.cuda.stream(stream):
         for i in range(3):
             step(i)
@@ -371,11 +385,19 @@ def run_ours(args, rank, world, dist):
                    f"({copies * w_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)"
                    if copies > 1 else
                    f"weights {w_bytes / 1e6:.0f} MB > 3x L2"),
-            "timing": f"CUDA graphs of {L} launches, {reps} replays"
-                      + (f" + {rem}" if rem else "") + ", events on stream",
+            "timing": f"CUDA graphs of {L} calls, {reps} replays"
+                      + (f" + {rem}" if rem else "") + ", events on stream"
+                      + ("; launch overlap on: a call's weights stream "
+                         "while the previous call finishes, its x is read "
+                         "after that call completes" if overlap else ""),
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
-        "gpu_launches": K,
+        "gpu_launches": K * launches_per_step,
+        "launch_overlap": overlap,
+        "serial": {"us_per_call": round(ms_serial * 1e3 / K, 3),
+                   "value": round(step_bytes * K * world / (ms_serial * 1e-3) / 1e9, 2),
+                   "note": "same steps with launch overlap off (each call "
+                           "starts after the previous one completes)"},
         "roofline": {
             "bound": "hbm",
             "achieved": round(step_bytes / (ms * 1e-3 / K) / 1e9, 2),
@@ -384,7 +406,8 @@ def run_ours(args, rank, world, dist):
             "frac": round(step_bytes / (ms * 1e-3 / K) / 1e9 / peak, 4),
             "traffic": traffic,
             "peak_source": f"{peak_kind} HBM copy bandwidth",
-            "kernel": "kq_set_direct",
+            "kernel": "kq_set_stream" if kernels["stream"] else "kq_set_direct",
+            "launches_per_step": launches_per_step,
         },
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -459,6 +482,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="headline with launch overlap off")
     ap.add_argument("--ref-rows-per-step", type=int, default=1)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -180,6 +180,14 @@ int kq_select_kernel(int which);
  */
 int kq_set_overlap(int enable);
 
+/*
+ * Kernels the calling thread's most recent successful kq_matvec /
+ * kq_matvec_set call enqueued, as bits: 1 = the direct-load kernel, 2 = the
+ * TMA-streaming kernel, 4 = the pass that writes input records to global
+ * memory first (when they do not fit in shared memory).  0 before any call.
+ */
+int kq_last_kernels(void);
+
 /* Library ABI version: (major << 16) | minor. */
 int kq_version(void);
 

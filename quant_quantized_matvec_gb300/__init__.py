@@ -145,6 +145,14 @@ def select_kernel(which: str) -> str:
     return {v: k for k, v in KERNELS.items()}[prev]
 
 
+def last_kernels() -> dict:
+    """Kernels enqueued by this thread's last successful call:
+    {"direct": bool, "stream": bool, "record_pass": bool}."""
+    b = _lib().kq_last_kernels()
+    return {"direct": bool(b & 1), "stream": bool(b & 2),
+            "record_pass": bool(b & 4)}
+
+
 def set_overlap(enable: bool) -> bool:
     """Let each streaming launch overlap the kernel before it on the stream
     (weights prefetched early; x read and y written only after that kernel

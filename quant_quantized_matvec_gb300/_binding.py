@@ -19,7 +19,7 @@ STATUS = {
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
            "kq_device_error", "kq_select_kernel", "kq_set_overlap",
-           "kq_version")
+           "kq_last_kernels", "kq_version")
 
 
 class KqMat(ctypes.Structure):
@@ -75,6 +75,8 @@ def load(path: str | None = None):
         lib.kq_select_kernel.restype = i32
         lib.kq_set_overlap.argtypes = [i32]
         lib.kq_set_overlap.restype = i32
+        lib.kq_last_kernels.argtypes = []
+        lib.kq_last_kernels.restype = i32
         lib.kq_version.argtypes = []
         lib.kq_version.restype = i32
         if path is None:

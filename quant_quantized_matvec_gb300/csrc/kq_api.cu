@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kPrepThreads) kq_xprep(const __grid_constant__
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+thread_local int g_last_kernels = 0;  // kq_last_kernels
 
 int64_t block_bytes_of(int fmt) {
     switch (fmt) {
@@ -266,6 +267,7 @@ kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
     }
+    g_last_kernels = 1 | 4;
     return KQ_OK;
 }
 
@@ -537,6 +539,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
     }
+    g_last_kernels = xsmem ? 2 : (2 | 4);
     return KQ_OK;
 }
 
@@ -651,6 +654,8 @@ int kq_select_kernel(int which) {
     if (which >= 0 && which <= 2) g_choice.store(which);
     return prev;
 }
+
+int kq_last_kernels(void) { return g_last_kernels; }
 
 int kq_set_overlap(int enable) {
     const int prev = g_overlap.load();

@@ -201,6 +201,9 @@ __host__ __device__ constexpr int stream_rows_per_task(int fmt, int ntok) {
 // What the consumer warps share.
 struct ConsumerCtx {
     uint8_t *smem;
+    const float *x;       // inputs (records are built from them in shared memory)
+    uint8_t *recs_w;      // shared-memory records to build
+    int *xissued;         // consumer warps whose input loads have gone out
     const uint8_t *recs;  // this member's input records (shared or global)
     float *part_f;
     int part_floats;      // floats per partial buffer
@@ -225,6 +228,15 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
     using XR = Rec<!XSMEM>;
     const int nb = c.nb;
     const int tstride = nb * REC;
+    if (XSMEM) {
+        build_records<Q6>(c.x, (int64_t)nb * 256, NTOK, nb, c.recs_w, warp, kStreamConsumers,
+                          lane, [&] {
+                              if (lane == 0)
+                                  asm volatile("red.relaxed.cta.shared::cta.add.u32 [%0], 1;" ::"r"(
+                                      smem_addr(c.xissued)));
+                          });
+        consumer_sync();
+    }
     int batch_base = 0;
     int slot = 0, lap = 0, g = 0, k = 0;
     int64_t g0 = c.G.start(0), g1 = c.G.start(1);
@@ -474,18 +486,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     // x (or its records) and y belong to the stream order: with an
     // overlapping launch, wait for the preceding kernel first.
     wait_prerequisites();
-    if (XSMEM) {
-        build_records(M.x, (int64_t)nb * 256, NTOK, nb, q6, smem + (recs - bars), warp,
-                      kStreamConsumers, lane, [&] {
-                          if (lane == 0)
-                              asm volatile("red.relaxed.cta.shared::cta.add.u32 [%0], 1;" ::"r"(
-                                  smem_addr(&xissued)));
-                      });
-        consumer_sync();
-    }
     ConsumerCtx c;
+    c.x = M.x;
+    c.xissued = &xissued;
     c.smem = smem;
     c.recs = XSMEM ? smem + (recs - bars) : M.rec;
+    c.recs_w = smem + (recs - bars);
     c.part_f = reinterpret_cast<float *>(smem + (parts - bars));
     c.part_floats = p.part_bytes / 8;
     c.bars = bars;

@@ -136,12 +136,13 @@ __device__ __forceinline__ float4 record_inputs(const float *x, int64_t cols, in
 // time: all loads of a batch are issued before any conversion.  `issued()`
 // is called once, as the first batch's loads go out (they are issued right
 // after it), so that the caller can start other memory traffic with them.
-constexpr int kRecBatch = 8;
+constexpr int kRecBatch = 5;
 
-template <class F>
+template <bool Q6, class F>
 __device__ __forceinline__ void build_records(const float *x, int64_t cols, int ntok, int nb,
-                                              bool q6, uint8_t *recs, int w, int nwarps,
-                                              int lane, F issued) {
+                                              uint8_t *recs, int w, int nwarps, int lane,
+                                              F issued) {
+    constexpr bool q6 = Q6;
     const int rb = rec_bytes(q6);
     const int n = nb * 2;  // halves per token
     bool first = true;
