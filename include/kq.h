@@ -57,7 +57,8 @@ typedef enum kq_status {
     KQ_ERR_ALIAS = 6,   /* an output overlaps an input or another output      */
     KQ_ERR_COUNT = 7,   /* set size outside 1..KQ_MAX_SET                     */
     KQ_ERR_CUDA = 8,    /* the CUDA launch failed (see kq_last_cuda_error)    */
-    KQ_ERR_TIMEOUT = 9  /* a bounded device-side wait expired                 */
+    KQ_ERR_TIMEOUT = 9, /* a bounded device-side wait expired                 */
+    KQ_ERR_LIMIT = 10   /* kq_matvec_noalloc: inputs beyond its fixed buffer  */
 } kq_status;
 
 #define KQ_MAX_NTOK 8
@@ -187,6 +188,33 @@ int kq_set_overlap(int enable);
  * memory first (when they do not fit in shared memory).  0 before any call.
  */
 int kq_last_kernels(void);
+
+/*
+ * kq_matvec without any memory allocation.  The pages have no counterpart:
+ * this is a library service for callers that must not allocate device
+ * memory during the call -- code running under a caller-managed memory
+ * budget or allocator that forbids hidden allocations, hot loops that must
+ * not take the allocator's locks or latency, and devices or processes where
+ * stream-ordered allocation (cudaMallocAsync) is unavailable.
+ *
+ * Same arguments, result and errors as kq_matvec, computed by the direct-
+ * load kernel with its input records (see the record pass) in one fixed
+ * file-scope device buffer of KQ_NOALLOC_RECORD_BYTES bytes instead of a
+ * stream-ordered temporary.  Calls whose records need more -- ntok * (cols
+ * / 256) * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K -- return
+ * KQ_ERR_LIMIT with nothing enqueued.  The records are written in full
+ * before they are read, so nothing in the buffer has to start at zero.
+ *
+ * The first call on a device looks the buffer up (cudaGetSymbolAddress,
+ * once per device); make that first call before any stream capture.  Every
+ * call shares the one buffer: calls that may overlap on the GPU (different
+ * streams, or different host threads without ordering) race and must be
+ * serialised by the caller.  Results are bitwise those of kq_matvec with
+ * the direct-load kernel.
+ */
+#define KQ_NOALLOC_RECORD_BYTES (1LL << 20)
+kq_status kq_matvec_noalloc(int fmt, const void *W, int64_t rows, int64_t cols,
+                            const float *x, float *y, int ntok, void *stream);
 
 /* Library ABI version: (major << 16) | minor. */
 int kq_version(void);

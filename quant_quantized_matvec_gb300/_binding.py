@@ -15,11 +15,12 @@ STATUS = {
     0: "KQ_OK", 1: "KQ_ERR_FORMAT", 2: "KQ_ERR_SHAPE", 3: "KQ_ERR_NTOK",
     4: "KQ_ERR_NULL", 5: "KQ_ERR_ALIGN", 6: "KQ_ERR_ALIAS",
     7: "KQ_ERR_COUNT", 8: "KQ_ERR_CUDA", 9: "KQ_ERR_TIMEOUT",
+    10: "KQ_ERR_LIMIT",
 }
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
            "kq_device_error", "kq_select_kernel", "kq_set_overlap",
-           "kq_last_kernels", "kq_version")
+           "kq_last_kernels", "kq_matvec_noalloc", "kq_version")
 
 
 class KqMat(ctypes.Structure):
@@ -63,6 +64,8 @@ def load(path: str | None = None):
         lib.kq_matrix_bytes.restype = i64
         lib.kq_matvec.argtypes = [i32, vp, i64, i64, vp, vp, i32, vp]
         lib.kq_matvec.restype = i32
+        lib.kq_matvec_noalloc.argtypes = [i32, vp, i64, i64, vp, vp, i32, vp]
+        lib.kq_matvec_noalloc.restype = i32
         lib.kq_matvec_set.argtypes = [ctypes.POINTER(KqMat), i32, i32, vp]
         lib.kq_matvec_set.restype = i32
         lib.kq_status_str.argtypes = [i32]

@@ -582,6 +582,91 @@ kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
     return run_direct(mats, n, ntok, s, info);
 }
 
+// ------------------------------------------------------------ no-alloc path
+// kq_matvec_noalloc: the direct-load path with its input records in one
+// fixed file-scope device buffer (KQ_NOALLOC_RECORD_BYTES), so the call
+// allocates nothing.  The buffer's address is looked up once per device.
+static __device__ __align__(256) uint8_t g_kq_noalloc_records[KQ_NOALLOC_RECORD_BYTES];
+
+cudaError_t noalloc_buffer(int dev, uint8_t **out) {
+    static std::mutex mu;
+    static uint8_t *addr[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_kq_noalloc_records);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<uint8_t *>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+kq_status run_noalloc(const kq_mat &m, int ntok, void *stream) {
+    const kq_status v = validate_set(&m, 1, ntok);
+    if (v != KQ_OK) return v;
+    const int nb = (int)(m.cols / 256);
+    const bool q6 = m.fmt == KQ_Q6_K;
+    const int64_t rec_total = (int64_t)ntok * nb * kq::rec_bytes(q6);
+    if (rec_total > KQ_NOALLOC_RECORD_BYTES) return KQ_ERR_LIMIT;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    DeviceInfo info;
+    if (e == cudaSuccess) e = device_info(dev, info);
+    uint8_t *buf = nullptr;
+    if (e == cudaSuccess) e = noalloc_buffer(dev, &buf);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+
+    // the record pass, into the fixed buffer
+    kq::PrepParams pp{};
+    pp.n = 1;
+    pp.ntok = ntok;
+    pp.x[0] = m.x;
+    pp.rec[0] = buf;
+    pp.nb[0] = nb;
+    pp.q6[0] = q6 ? 1 : 0;
+    pp.first_warp[0] = 0;
+    pp.first_warp[1] = (int64_t)ntok * nb * 2;
+    const int64_t blocks = (pp.first_warp[1] * 32 + kq::kPrepThreads - 1) / kq::kPrepThreads;
+
+    // the direct kernel's plan (rows per CTA as in run_direct)
+    kq::SetParams p{};
+    p.n = 1;
+    int64_t rpc = std::max<int64_t>(1, kq::kDirectThreads / nb);
+    rpc = std::min<int64_t>(rpc, 32);
+    rpc = std::min<int64_t>(rpc, std::max<int64_t>(1, (m.rows + info.sms - 1) / info.sms));
+    const int64_t per_row = (int64_t)nb * ntok * (int64_t)sizeof(float);
+    rpc = std::min<int64_t>(rpc, std::max<int64_t>(1, kSmemLimit / per_row));
+    if (per_row * rpc > kSmemLimit) return KQ_ERR_SHAPE;
+    const int64_t grid = (m.rows + rpc - 1) / rpc;
+    if (grid > 0x7FFFFFFF) return KQ_ERR_SHAPE;
+    p.m[0].W = (const uint8_t *)m.W;
+    p.m[0].x = m.x;
+    p.m[0].rec = buf;
+    p.m[0].y = m.y;
+    p.m[0].rows = m.rows;
+    p.m[0].nb = nb;
+    p.m[0].fmt = m.fmt;
+    p.m[0].cta_begin = 0;
+    p.m[0].rpc = (int32_t)rpc;
+
+    kq::kq_xprep<<<(unsigned)blocks, kq::kPrepThreads, 0, s>>>(pp);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = kqlaunch::direct(ntok, p, (int)grid, (size_t)(per_row * rpc), s);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    g_last_kernels = 1 | 4;
+    return KQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -613,6 +698,19 @@ kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream) {
     return run_set(mats, n, ntok, stream);
 }
 
+kq_status kq_matvec_noalloc(int fmt, const void *W, int64_t rows, int64_t cols,
+                            const float *x, float *y, int ntok, void *stream) {
+    kq_mat m;
+    m.fmt = fmt;
+    m.reserved = 0;
+    m.W = W;
+    m.rows = rows;
+    m.cols = cols;
+    m.x = x;
+    m.y = y;
+    return run_noalloc(m, ntok, stream);
+}
+
 const char *kq_status_str(int status) {
     switch (status) {
     case KQ_OK: return "ok";
@@ -625,6 +723,7 @@ const char *kq_status_str(int status) {
     case KQ_ERR_COUNT: return "set size outside 1..16";
     case KQ_ERR_CUDA: return "CUDA launch failed";
     case KQ_ERR_TIMEOUT: return "device-side wait timed out";
+    case KQ_ERR_LIMIT: return "inputs exceed the fixed buffer of kq_matvec_noalloc";
     default: return "unknown status";
     }
 }

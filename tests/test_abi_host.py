@@ -134,3 +134,19 @@ def test_stage_task_division_is_exact():
         hinv = ((1 << 20) + hp - 1) // hp
         for t in range(4096):
             assert ((t * hinv) & 0xFFFFFFFF) >> 20 == t // hp, (hp, t)
+
+
+def test_noalloc_validates_before_any_cuda_call():
+    """kq_matvec_noalloc checks its arguments and its buffer limit on the
+    host: these calls return without touching the (absent) GPU."""
+    lib = _binding.load()
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced
+    assert lib.kq_matvec_noalloc(99, fake, 4, 256, fake, ctypes.c_void_p(1 << 24), 1,
+                                 None) == 1  # KQ_ERR_FORMAT
+    assert lib.kq_matvec_noalloc(14, fake, 4, 255, fake, ctypes.c_void_p(1 << 24), 1,
+                                 None) == 2  # KQ_ERR_SHAPE
+    # Q6_K records for ntok=8, cols=256*125: 8*125*1056 > 1 MiB
+    assert lib.kq_matvec_noalloc(14, ctypes.c_void_p(1 << 30), 2, 256 * 125,
+                                 ctypes.c_void_p(1 << 34), ctypes.c_void_p(1 << 36), 8,
+                                 None) == 10  # KQ_ERR_LIMIT
+    assert lib.kq_status_str(10).decode().startswith("inputs exceed")
