@@ -40,6 +40,7 @@ constexpr int kStreamConsumers = 12;
 constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
 constexpr int kMaxMaps = 4;
 constexpr int kMaxSlots = 32;
+constexpr int kMaxHinv = 40;  // row-pair offsets hp of a stage are at most 17
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 struct StreamMember {
@@ -53,6 +54,9 @@ struct StreamMember {
     int32_t cta_begin;
     int32_t ncta;
     int32_t rows_q, rows_r;  // rows / ncta, rows % ncta
+    // row groups of a CTA with rows_q rows ([0]) or rows_q + 1 rows ([1]):
+    // ng groups of gq or gq + 1 rows (the first gr one more)
+    int32_t ng[2], gq[2], gr[2];
     int32_t rmax;   // rows per group at most
     int32_t kb;     // blocks per box (Q4_K / Q5_K)
     int32_t nmaps;  // tensor maps (box heights) for this member
@@ -68,6 +72,7 @@ struct StreamParams {
     int32_t x_bytes;     // input records in shared memory (0: in global memory)
     int32_t part_bytes;
     int32_t overlap;     // launched to overlap the preceding kernel
+    uint32_t hinv[kMaxHinv + 1];  // ceil(2^20 / hp): t / hp = (t * hinv[hp]) >> 20
     unsigned int *err;   // device error word (nonzero: a wait expired)
 };
 
@@ -103,12 +108,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 // Wait for the phase of `parity` to complete; false once the wall-time limit
-// passes.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// passes.  Between polls the thread sleeps, doubling from 32 ns up to
+// `max_ns`, so that waiting warps leave the issue slots to working ones.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned max_ns = 256) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    while (!mbar_try(bar, parity))
+    unsigned ns = 32;
+    while (!mbar_try(bar, parity)) {
+        __nanosleep(ns);
+        if (ns < max_ns) ns <<= 1;
         if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
     return true;
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src,
@@ -147,8 +158,10 @@ struct Q6WordsShared {
     const uint8_t *a4;  // block start rounded down to 4 bytes
     uint32_t sh;        // 8 * (block start - a4)
     static __device__ __forceinline__ Q6WordsShared at(const uint8_t *p) {
-        const uintptr_t u = reinterpret_cast<uintptr_t>(p);
-        return {reinterpret_cast<const uint8_t *>(u & ~(uintptr_t)3), (uint32_t)(u & 3u) * 8u};
+        // pointer arithmetic (not an integer round trip) keeps the
+        // shared-memory address space visible, so the loads stay LDS
+        const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(p) & 3u;
+        return {p - mis, mis * 8u};
     }
     __device__ __forceinline__ void words4(int j, uint32_t (&o)[4]) const {
         uint32_t r[5];
@@ -171,14 +184,17 @@ struct Groups {
     __device__ __forceinline__ int64_t start(int g) const {
         return ra + (int64_t)(g * gq + (g < gr ? g : gr));
     }
-    // CTA cidx of a member whose rows split into ncta CTAs of rows_q or
-    // rows_q + 1 rows (the first rows_r CTAs one more)
-    __device__ __forceinline__ void init(int cidx, int rows_q, int rows_r, int rmax) {
-        ra = (int64_t)cidx * rows_q + (cidx < rows_r ? cidx : rows_r);
-        n = rows_q + (cidx < rows_r ? 1 : 0);
-        ng = (n + rmax - 1) / rmax;
-        gq = n / ng;
-        gr = n - gq * ng;
+    // CTA cidx of member M, whose rows split into ncta CTAs of rows_q or
+    // rows_q + 1 rows (the first rows_r CTAs one more); group splits are
+    // precomputed on the host for both sizes
+    template <class MEM>
+    __device__ __forceinline__ void init(int cidx, const MEM &M) {
+        const int big = cidx < M.rows_r ? 1 : 0;
+        ra = (int64_t)cidx * M.rows_q + (big ? cidx : M.rows_r);
+        n = M.rows_q + big;
+        ng = M.ng[big];
+        gq = M.gq[big];
+        gr = M.gr[big];
     }
 };
 
@@ -215,6 +231,7 @@ struct ConsumerCtx {
     Groups G;
     int *abort_flag;
     int *gcount;
+    const uint32_t *hinv;  // ceil(2^20 / hp) by hp
     unsigned int *err;
 };
 
@@ -238,17 +255,18 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         consumer_sync();
     }
     int batch_base = 0;
+    int rot = 0;  // batch_base % kStreamConsumers
     int slot = 0, lap = 0, g = 0, k = 0;
     int64_t g0 = c.G.start(0), g1 = c.G.start(1);
     int h = (int)(g1 - g0);
     int hp = R == 2 ? pair_offset<Q6>(h, nb) : h;
-    uint32_t hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
+    uint32_t hinv = c.hinv[hp];
 #pragma unroll 1
     for (int s = 0; s < c.nstage; ++s) {
         const int b0 = Q6 ? 0 : k * c.kb;
         const int kbv = Q6 ? nb : (nb - b0 < c.kb ? nb - b0 : c.kb);
         const int tasks = hp * kbv;
-        const int nbat = (tasks + 31) / 32;
+        const int nbat = (int)(((uint32_t)tasks + 31u) >> 5);
         const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
         float *pbuf = c.part_f + (g & 1) * c.part_floats;
         bool ok = !*(volatile int *)c.abort_flag;
@@ -257,7 +275,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             atomicOr(c.err, 1u);
             ok = false;
         }
-        if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1)) {
+        if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1, 128)) {
             atomicExch(c.abort_flag, 1);
             atomicOr(c.err, 1u);
             ok = false;
@@ -265,8 +283,10 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         if (ok) {
             // byte offset of the group's first row inside the slot (Q6_K)
             const uint32_t q6off = Q6 ? (uint32_t)((g0 * c.row_bytes) & 15) : 0u;
-            int bat = batch_base + ((warp - batch_base % kStreamConsumers) + kStreamConsumers) %
-                                       kStreamConsumers;
+            // this warp's first batch: the one dealt to it in the rotation
+            int dw = warp - rot;
+            if (dw < 0) dw += kStreamConsumers;
+            int bat = batch_base + dw;
 #pragma unroll 1
             for (; bat < batch_base + nbat; bat += kStreamConsumers) {
                 // Lanes past the stage's last task redo the last task and do
@@ -307,6 +327,8 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             }
         }
         batch_base += nbat;
+        rot += nbat;
+        while (rot >= kStreamConsumers) rot -= kStreamConsumers;
         __syncwarp();
         if (lane == 0) mbar_arrive(c.bars + 8 * (kMaxSlots + slot));
 
@@ -349,11 +371,8 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             g0 = g1;
             g1 = c.G.start(g + 1);
             h = (int)(g1 - g0);
-            const int hp_next = h < 1 ? 1 : (R == 2 ? pair_offset<Q6>(h, nb) : h);
-            if (hp_next != hp) {
-                hp = hp_next;
-                hinv = ((1u << 20) + (uint32_t)hp - 1) / (uint32_t)hp;
-            }
+            hp = h < 1 ? 1 : (R == 2 ? pair_offset<Q6>(h, nb) : h);
+            hinv = c.hinv[hp];
         }
     }
 }
@@ -377,7 +396,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int64_t row_bytes = (int64_t)nb * bb;
     const int cidx = (int)blockIdx.x - M.cta_begin;
     Groups G;
-    G.init(cidx, M.rows_q, M.rows_r, M.rmax);
+    G.init(cidx, M);
     const bool q6 = fmt == kFmtQ6K;
     const int nbox = q6 ? 1 : (nb + M.kb - 1) / M.kb;
     const int nstage = G.ng * nbox;
@@ -416,6 +435,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (XSMEM && !p.overlap) {
             const unsigned long long t0 = global_ns();
             while (*(volatile int *)&xissued < kStreamConsumers) {
+                __nanosleep(20);
                 if (global_ns() - t0 > kWaitLimitNs) {
                     atomicExch(&abort_flag, 1);
                     atomicOr(p.err, 1u);
@@ -510,6 +530,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.abort_flag = &abort_flag;
     c.gcount = gcount;
     c.err = p.err;
+    c.hinv = p.hinv;
     if (fmt == kFmtQ4K)
         consume<NTOK, XSMEM, kFmtQ4K>(c, warp, lane);
     else if (fmt == kFmtQ5K)
