@@ -40,6 +40,7 @@ constexpr int kStreamConsumers = 12;
 constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
 constexpr int kMaxMaps = 4;
 constexpr int kMaxSlots = 32;
+constexpr int kOverlapPrefetch = 1;  // stages issued before the inputs (overlap)
 constexpr int kMaxHinv = 40;  // row-pair offsets hp of a stage are at most 17
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -427,12 +428,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     if (warp == kStreamConsumers) {
         // ------------------------------------------------ producer
         if (lane != 0) return;
-        // The consumers' input loads go out with the first weight requests,
-        // not queued behind the weight stream: wait until every consumer
-        // warp is about to issue them (a relaxed counter).  Not when the
-        // launch overlaps the preceding kernel: then the weights stream
-        // while the consumers wait for that kernel.
-        if (XSMEM && !p.overlap) {
+        // The consumers' input loads must not queue behind the weight
+        // stream.  The producer issues `gate` stages, then waits until every
+        // consumer warp is about to issue its input loads (a relaxed
+        // counter) before it issues the rest.  gate = 0 for an ordinary
+        // launch; with launch overlap a few stages go out first, while the
+        // consumers still wait for the preceding kernel.
+        const int gate = XSMEM ? (p.overlap ? kOverlapPrefetch : 0) : -1;
+        auto wait_inputs_issued = [&]() {
             const unsigned long long t0 = global_ns();
             while (*(volatile int *)&xissued < kStreamConsumers) {
                 __nanosleep(20);
@@ -442,11 +445,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     break;
                 }
             }
-        }
+        };
+        if (gate == 0) wait_inputs_issued();
         int issued = 0;
         int slot = 0, lap = 0, g = 0, k = 0;
         int64_t g0 = G.start(0), g1 = G.start(1);
         for (int s = 0; s < nstage; ++s) {
+            if (s == gate && s > 0) wait_inputs_issued();
             if (*(volatile int *)&abort_flag) break;
             if (s >= nslot) {
                 if (!mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1)) {
