@@ -8,7 +8,8 @@ A step is one pass of the whole hot path over one batch of synthetic input:
 by default the Muse Glimmer QKV+gate concurrent set at ntok=1 (Q and gate
 4096x6656 Q4_K, K and V 256x6656 Q6_K, one shared x) in ONE kq_matvec_set
 launch.  Other workloads (--workload) time the single-matrix shapes, the
-Q6_K+Q5_K grid-split pair and the LM head.
+Q6_K+Q5_K grid-split pair, the LM head and the embedding lookup (embed_q4k:
+--ntok token rows of a 202048x6656 Q4_K table per step, kq_dequant_rows).
 
 Timing (ours): inputs resident in HBM; K steps replayed from CUDA graphs,
 bracketed by CUDA events on the launching stream with a barrier and a device
@@ -72,6 +73,10 @@ def workload(name: str, ntok: int):
                 "grid-split pair Q6_K + Q5_K 2560->512, separate x planes")
     if name == "lm_head_q6k":
         return ([(Q6_K, 202048, 6656, 0)], "LM head Q6_K 202048x6656")
+    if name == "embed_q4k":
+        return ([(Q4_K, 202048, 6656, 0)],
+                "embedding lookup: ntok token rows of a 202048x6656 Q4_K table "
+                "gathered and dequantized to f32 (kq_dequant_rows)")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -422,6 +427,140 @@ def run_ours(args, rank, world, dist):
     return line
 
 
+# ----------------------------------------------------------------- embedding
+def run_embed(args, rank, world, dist):
+    """The embedding lookup: ntok random token rows per step, gathered and
+    dequantized by kq_dequant_rows; bytes = rows read + ids + f32 rows
+    written."""
+    import torch
+
+    import quant_quantized_matvec_gb300 as kq
+    from quant_quantized_matvec_gb300 import build as kbuild
+    kbuild.build()
+    kq._binding.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    (fmt, rows, cols, _), = workload(args.workload, args.ntok)[0]
+    n = args.ntok
+    W = synth.kquant_matrix(fmt, rows, cols, f"bench/{args.workload}/W")
+    Wd = torch.from_numpy(W.reshape(-1)).to(dev)
+    row_bytes = (cols // 256) * synth.BLOCK_BYTES[fmt]
+    step_bytes = n * row_bytes + 4 * n + 4 * n * cols
+    K = args.steps
+    L = min(K, args.graph_len)
+    rng = np.random.default_rng(1)
+    ids_all = torch.from_numpy(
+        rng.integers(0, rows, size=(L, n)).astype(np.int32)).to(dev)
+    out = torch.empty((n, cols), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        kq.dequant_rows(fmt, Wd, rows, cols, ids_all[i % L], out=out,
+                        stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(L):
+            step(i)
+    reps, rem = K // L, K % L
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                step(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+        if g_rem is not None:
+            g_rem.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    gbs = step_bytes * K * world / (ms * 1e-3) / 1e9
+    # end to end: ids from pinned host memory, rows back to pinned host memory
+    ids_host = torch.from_numpy(
+        rng.integers(0, rows, size=n).astype(np.int32)).pin_memory()
+    ids_dev = torch.empty(n, dtype=torch.int32, device=dev)
+    out_host = torch.empty((n, cols), dtype=torch.float32).pin_memory()
+    Ke = min(K, args.e2e_steps)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(Ke):
+            ids_dev.copy_(ids_host, non_blocking=True)
+            kq.dequant_rows(fmt, Wd, rows, cols, ids_dev, out=out, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = e0.elapsed_time(e1)
+    peak, peak_kind = peaks()
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms / K, 6), "us_per_call": round(ms * 1e3 / K, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded Q4_K table, random token ids)",
+        "config": {"workload": args.workload,
+                   "description": workload(args.workload, n)[1],
+                   "ntok": n, "bytes_per_step": step_bytes,
+                   "l2": f"table {W.nbytes / 1e6:.0f} MB > 3x L2; random rows",
+                   "timing": f"CUDA graphs of {L} calls, events on stream",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm",
+                     "achieved": round(step_bytes / (ms * 1e-3 / K) / 1e9, 2),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(step_bytes / (ms * 1e-3 / K) / 1e9 / peak, 4),
+                     "traffic": None,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "kernel": "kq_rows_kernel", "launches_per_step": 1},
+        "e2e": {"value": round(step_bytes * Ke / (ems * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": 4 * n,
+                "d2h_bytes_per_step": 4 * n * cols,
+                "us_per_step": round(ems * 1e3 / Ke, 3), "steps": Ke,
+                "weights": "resident in HBM"},
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        t0, done, reps_c = time.perf_counter(), 0, 0
+        while time.perf_counter() - t0 < args.cpu_budget:
+            idx = rng.integers(0, rows, size=n).tolist()
+            oracle.dequant_rows(fmt, W, cols, rows=idx)
+            done += step_bytes
+            reps_c += 1
+        el = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": round(done / el / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps_c} lookups of {n} random rows, {el:.1f} s "
+                      "single-threaded (oracle dequantizer)"}
+    return line
+
+
 # ----------------------------------------------------------------- reference
 def run_reference(args):
     """The CPU oracle as the reference arm: each step evaluates a bounded row
@@ -433,8 +572,14 @@ def run_reference(args):
     Ws, planes = host_inputs(members, ntok, f"bench/{args.workload}")
     rows_per_step = args.ref_rows_per_step
     cursor = [0] * len(members)
+    embed = args.workload == "embed_q4k"
+    rng = np.random.default_rng(1)
 
     def step():
+        if embed:  # the lookup itself: ntok random rows per step
+            f, r, c, _ = members[0]
+            oracle.dequant_rows(f, Ws[0], c, rows=rng.integers(0, r, size=ntok).tolist())
+            return ntok * ((c // 256) * synth.BLOCK_BYTES[f] + 4 + 4 * c)
         nbytes = 0
         for i, (f, r, c, p) in enumerate(members):
             idx = (cursor[i] + np.arange(rows_per_step)) % r
@@ -504,7 +649,10 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
         dist = tdist
-    line = run_ours(args, rank, world, dist)
+    if args.workload == "embed_q4k":
+        line = run_embed(args, rank, world, dist)
+    else:
+        line = run_ours(args, rank, world, dist)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

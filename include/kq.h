@@ -138,6 +138,29 @@ typedef struct kq_mat {
  */
 kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream);
 
+/*
+ * Rows of a K-quant matrix gathered by index and dequantized to f32 -- the
+ * embedding lookup ("Chapter 6 - The kquant family on the reference lane",
+ * section 6.7, muser_embedding_q4k: the token's row of the Q4_K embedding
+ * table, dequantized element by element with section 6.3's formula), for
+ * any of the three formats:
+ *
+ *   out[i][j] = W[ids[i], j],  i < n, j < cols
+ *
+ *   fmt, W, rows, cols  as kq_matvec (W device, 16-byte aligned).
+ *   ids   device int32[n]; an index outside [0, rows) yields a row of NaN.
+ *   n     rows to gather, 0..2^31-1 (0: nothing is enqueued).
+ *   out   device f32 [n][cols], 16-byte aligned, overwritten; must not
+ *         overlap W or ids.
+ *
+ * Each value is the correctly rounded weight: d*sc*q - dmin*m (Q4_K,
+ * Q5_K) or d*sc*(q-32) (Q6_K) with only the final subtraction rounded
+ * (the products are exact in f32), so any exact evaluation gives the same
+ * bits.  Validation and status codes as kq_matvec.
+ */
+kq_status kq_dequant_rows(int fmt, const void *W, int64_t rows, int64_t cols,
+                          const int32_t *ids, int64_t n, float *out, void *stream);
+
 /* Static English text for a status code (never NULL). */
 const char *kq_status_str(int status);
 

@@ -91,6 +91,28 @@ def matvec(fmt, W, rows, cols, x, y=None, stream=None):
     return y.view(rows) if squeeze and y.dim() == 2 and ntok == 1 else y
 
 
+def dequant_rows(fmt, W, rows, cols, ids, out=None, stream=None):
+    """Rows ids of the K-quant matrix W, dequantized to f32 [len(ids), cols]
+    (the embedding lookup).  ids: int32 tensor on the device."""
+    import torch
+    _check_tensor(W, "W")
+    _check_tensor(ids, "ids", torch.int32)
+    n = ids.numel()
+    if W.numel() * W.element_size() != matrix_bytes(fmt, rows, cols):
+        raise ValueError("W size does not match fmt/rows/cols")
+    if out is None:
+        out = torch.empty((n, cols), dtype=torch.float32, device=W.device)
+    _check_tensor(out, "out", torch.float32)
+    if out.numel() != n * cols:
+        raise ValueError("out must hold len(ids)*cols floats")
+    st = _lib().kq_dequant_rows(int(fmt), W.data_ptr(), int(rows), int(cols),
+                                ids.data_ptr(), int(n), out.data_ptr(),
+                                _stream_ptr(stream))
+    if st != 0:
+        raise KQError(st, "kq_dequant_rows")
+    return out
+
+
 def make_set(members):
     """members: iterable of (fmt, W, rows, cols, x, y) with torch tensors.
     Returns a ctypes array of kq_mat descriptors (reusable across calls)."""

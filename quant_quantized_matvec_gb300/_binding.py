@@ -20,7 +20,8 @@ STATUS = {
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
            "kq_device_error", "kq_select_kernel", "kq_set_overlap",
-           "kq_last_kernels", "kq_matvec_noalloc", "kq_version")
+           "kq_last_kernels", "kq_matvec_noalloc", "kq_dequant_rows",
+           "kq_version")
 
 
 class KqMat(ctypes.Structure):
@@ -64,6 +65,8 @@ def load(path: str | None = None):
         lib.kq_matrix_bytes.restype = i64
         lib.kq_matvec.argtypes = [i32, vp, i64, i64, vp, vp, i32, vp]
         lib.kq_matvec.restype = i32
+        lib.kq_dequant_rows.argtypes = [i32, vp, i64, i64, vp, i64, vp, vp]
+        lib.kq_dequant_rows.restype = i32
         lib.kq_matvec_noalloc.argtypes = [i32, vp, i64, i64, vp, vp, i32, vp]
         lib.kq_matvec_noalloc.restype = i32
         lib.kq_matvec_set.argtypes = [ctypes.POINTER(KqMat), i32, i32, vp]

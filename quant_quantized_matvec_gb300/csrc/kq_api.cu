@@ -737,6 +737,30 @@ kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream) {
     return run_set(mats, n, ntok, stream);
 }
 
+kq_status kq_dequant_rows(int fmt, const void *W, int64_t rows, int64_t cols,
+                          const int32_t *ids, int64_t n, float *out, void *stream) {
+    const int64_t bb = block_bytes_of(fmt);
+    if (bb < 0) return KQ_ERR_FORMAT;
+    if (rows < 1 || rows > KQ_MAX_ROWS || cols < 256 || cols % 256 != 0 || cols > KQ_MAX_COLS ||
+        n < 0 || n > 0x7FFFFFFF)
+        return KQ_ERR_SHAPE;
+    if (n == 0) return KQ_OK;
+    if (!W || !ids || !out) return KQ_ERR_NULL;
+    if (((uintptr_t)W & 15u) || ((uintptr_t)out & 15u) || ((uintptr_t)ids & 3u))
+        return KQ_ERR_ALIGN;
+    const Range ro{(uintptr_t)out, (uintptr_t)out + (uintptr_t)(n * cols * (int64_t)sizeof(float))};
+    const Range rw{(uintptr_t)W, (uintptr_t)W + (uintptr_t)(rows * (cols / 256) * bb)};
+    const Range ri{(uintptr_t)ids, (uintptr_t)ids + (uintptr_t)(n * (int64_t)sizeof(int32_t))};
+    if (overlaps(ro, rw) || overlaps(ro, ri)) return KQ_ERR_ALIAS;
+    const cudaError_t e = kqlaunch::rows(fmt, (const uint8_t *)W, rows, (int)(cols / 256), ids, n,
+                                         out, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    return KQ_OK;
+}
+
 kq_status kq_matvec_noalloc(int fmt, const void *W, int64_t rows, int64_t cols,
                             const float *x, float *y, int ntok, void *stream) {
     kq_mat m;

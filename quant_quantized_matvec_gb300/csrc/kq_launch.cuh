@@ -70,6 +70,10 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
     return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM>, p);
 }
 
+// Row gather + dequantization (kq_rows.cu).
+cudaError_t rows(int fmt, const uint8_t *W, int64_t rows, int nb, const int32_t *ids, int64_t n,
+                 float *out, cudaStream_t s);
+
 // ntok-dispatching entry points (defined in kq_api.cu from the instances)
 cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,

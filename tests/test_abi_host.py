@@ -150,3 +150,15 @@ def test_noalloc_validates_before_any_cuda_call():
                                  ctypes.c_void_p(1 << 34), ctypes.c_void_p(1 << 36), 8,
                                  None) == 10  # KQ_ERR_LIMIT
     assert lib.kq_status_str(10).decode().startswith("inputs exceed")
+
+
+def test_dequant_rows_validates_before_any_cuda_call():
+    lib = _binding.load()
+    W, ids, out = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 24), ctypes.c_void_p(1 << 28)
+    assert lib.kq_dequant_rows(99, W, 4, 256, ids, 1, out, None) == 1   # format
+    assert lib.kq_dequant_rows(12, W, 4, 300, ids, 1, out, None) == 2   # cols % 256
+    assert lib.kq_dequant_rows(12, W, 4, 256, ids, -1, out, None) == 2  # n < 0
+    assert lib.kq_dequant_rows(12, W, 4, 256, None, 0, None, None) == 0  # n = 0: nothing to do
+    assert lib.kq_dequant_rows(12, W, 4, 256, None, 1, out, None) == 4  # null ids
+    assert lib.kq_dequant_rows(12, W, 4, 256, ids, 1, ctypes.c_void_p((1 << 28) + 4), None) == 5
+    assert lib.kq_dequant_rows(12, W, 4, 256, ids, 1, ctypes.c_void_p((1 << 20) + 16), None) == 6
