@@ -73,6 +73,24 @@ def workload(name: str, ntok: int):
                 "grid-split pair Q6_K + Q5_K 2560->512, separate x planes")
     if name == "lm_head_q6k":
         return ([(Q6_K, 202048, 6656, 0)], "LM head Q6_K 202048x6656")
+    # further release shapes ("Chapter 6 - The kquant family on the
+    # reference lane", Figure 6.6; n_in -> n_out is cols -> rows)
+    if name == "ffn_gate_up_set":
+        return ([(Q4_K, 19968, 6656, 0), (Q4_K, 19968, 6656, 0)],
+                "FFN gate + up concurrent set: 2 x Q4_K 6656->19968, shared x")
+    if name == "ffn_down_q4k":
+        return ([(Q4_K, 6656, 19968, 0)], "FFN down Q4_K 19968->6656")
+    if name == "ffn_down_q6k":
+        return ([(Q6_K, 6656, 19968, 0)], "FFN down Q6_K 19968->6656")
+    if name == "attn_output_q4k":
+        return ([(Q4_K, 6656, 4096, 0)], "attention output Q4_K 4096->6656")
+    if name == "lm_head_q5k":
+        return ([(Q5_K, 202048, 6656, 0)], "LM head Q5_K 6656->202048")
+    if name == "draft_kv_set":
+        return ([(Q4_K, 1024, 6656, 0), (Q6_K, 1024, 6656, 0)],
+                "draft k + v set: Q4_K and Q6_K 6656->1024, shared x")
+    if name == "draft_fc_q4k":
+        return ([(Q4_K, 6656, 33280, 0)], "draft fc Q4_K 33280->6656")
     if name == "embed_q4k":
         return ([(Q4_K, 202048, 6656, 0)],
                 "embedding lookup: ntok token rows of a 202048x6656 Q4_K table "
