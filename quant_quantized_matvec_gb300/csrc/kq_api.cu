@@ -403,14 +403,14 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         --used;
     }
 
-    // Stage geometry, from the largest stages down ("levels"): Q4_K / Q5_K
-    // stages are [h rows][kb blocks] boxes with h <= rcap and box rows of at
-    // most kb_bytes; Q6_K stages are a few whole rows, as many as fit the
-    // slot size the other members need (or 64 KiB >> level when every member
-    // is Q6_K).  The first level whose input records fit in shared memory
-    // beside at least three slots (two at the smallest level, or when a CTA
-    // has only two stages) is taken; if none fits, level 0 with the records
-    // in global memory.
+    // Stage geometry, from the largest stages down ("levels"): stages are
+    // [h rows][kb blocks] with h <= rcap and stage rows of at most kb_bytes
+    // (Q6_K row segments sit seg bytes apart in the slot, seg = 16 * odd so
+    // that rows start on different bank groups, with room for the segment's
+    // misalignment at both ends).  The first level whose input records fit
+    // in shared memory beside at least three slots (two at the smallest
+    // level, or when a CTA has only two stages) is taken; if none fits,
+    // level 0 with the records in global memory.
     static const int kLevelRcap[] = {32, 16, 16, 8, 8};
     static const int kLevelKbBytes[] = {2048, 2048, 1024, 1024, 512};
     constexpr int kLevels = 5;
@@ -421,15 +421,6 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     bool xsmem = false;
     auto plan = [&](int level) -> kq_status {
         const int rcap = kLevelRcap[level], kb_bytes = kLevelKbBytes[level];
-        int64_t slot45 = 0;
-        for (int i = 0; i < n; ++i) {
-            if (mats[i].fmt == KQ_Q6_K) continue;
-            const int nb = (int)(mats[i].cols / 256);
-            const int bb = (int)block_bytes_of(mats[i].fmt);
-            const int kbmax = (int)std::max<int64_t>(1, std::min<int64_t>(nb, kb_bytes / bb));
-            slot45 = std::max<int64_t>(slot45, (int64_t)rcap * kbmax * bb);
-        }
-        const int64_t q6_target = slot45 > 0 ? slot45 : (64 * 1024) >> level;
         x_bytes = part_bytes = slot_bytes = stages = 0;
         cta = 0;
         for (int i = 0; i < n; ++i) {
@@ -452,10 +443,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
             cta += ncta[i];
             // rows per group: partials for the group must fit in 64 KiB
             const int64_t part_row = (int64_t)nb * ntok * 4;
-            int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
-            if (m.fmt == KQ_Q6_K)
-                rmax = (int)std::min<int64_t>(
-                    rmax, std::max<int64_t>(1, std::min<int64_t>(16, (q6_target - 32) / row_bytes)));
+            const int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
             if (rmax < 1) return KQ_ERR_SHAPE;
             M.rmax = rmax;
             for (int big = 0; big < 2; ++big) {  // CTAs of rows_q / rows_q + 1 rows
@@ -502,14 +490,11 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
             // tasks of a stage (row pairs x block columns) stay below 2^12, the
             // range of the kernel's multiply-shift division
             {
-                int hp = hmax;
-                if (kq::stream_rows_per_task(m.fmt, ntok) == 2) {
-                    hp = (hmax + 1) / 2;
-                    if (m.fmt == KQ_Q6_K && (nb & 1) && (hp & 1) && hmax > 1) ++hp;
-                }
-                if ((int64_t)hp * (m.fmt == KQ_Q6_K ? nb : M.kb) >= 4096) return KQ_ERR_SHAPE;
+                const int hp = kq::stream_rows_per_task(m.fmt, ntok) == 2 ? (hmax + 1) / 2 : hmax;
+                if ((int64_t)hp * M.kb >= 4096) return KQ_ERR_SHAPE;
             }
             M.nmaps = m.fmt == KQ_Q6_K ? 0 : nh;
+            M.seg = 0;
             if (m.fmt != KQ_Q6_K) {
                 const int box_w = (int)(M.kb * bb / 8);
                 for (int j = 0; j < nh; ++j) {
@@ -519,12 +504,16 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
                 }
                 slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * M.kb * bb);
             } else {
-                slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * row_bytes + 32);
+                // a segment of kb blocks starts up to 14 bytes past a 16-byte
+                // boundary and its copy ends up to 14 bytes past its end
+                int seg = (int)round_up((int64_t)M.kb * 210 + 28, 16);
+                if (((seg / 16) & 1) == 0) seg += 16;
+                M.seg = seg;
+                slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * seg);
             }
             // stages of this member's largest CTA
-            stages = std::max<int64_t>(
-                stages, (int64_t)M.ng[M.rows_r > 0 ? 1 : 0] *
-                            (m.fmt == KQ_Q6_K ? 1 : (nb + M.kb - 1) / M.kb));
+            stages = std::max<int64_t>(stages, (int64_t)M.ng[M.rows_r > 0 ? 1 : 0] *
+                                                   ((nb + M.kb - 1) / M.kb));
             // input records [ntok][nb] (kq_xrec.cuh)
             x_bytes = std::max<int64_t>(x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
             part_bytes = std::max<int64_t>(part_bytes, (int64_t)hmax * part_row);

@@ -1,16 +1,17 @@
 // kq_kernel_stream.cuh -- the set kernel, TMA-streaming variant.
 //
 // One CTA per SM.  Each CTA owns a balanced, contiguous row range of one
-// member of the set, split into row groups of at most 32 rows (Q4_K, Q5_K)
-// or a few rows (Q6_K, whose rows are long).  A producer warp streams the
+// member of the set, split into row groups of at most 32 rows.  A producer
+// warp streams the
 // weights through a ring of shared-memory slots:
 //   * Q4_K / Q5_K: one 2-D tensor-map box per stage, [h rows][kb blocks]
 //     (kb chosen so that a box row is an odd number of 16-byte units and
 //     rows land on distinct shared-memory banks), cp.async.bulk.tensor;
-//   * Q6_K: the group's whole rows, which are contiguous in memory but only
-//     2-byte aligned, as 16-byte-aligned bulk copies (cp.async.bulk) of at
-//     most 32 KiB, the sub-16-byte tail at the end of the matrix copied by
-//     the producer with plain loads.
+//   * Q6_K: rows are only 2-byte aligned (no tensor map), so the same
+//     [h rows][kb blocks] stage is one 16-byte-aligned bulk copy
+//     (cp.async.bulk) per row segment, segments M.seg bytes apart, the
+//     sub-16-byte tail at the end of the matrix copied by the producer with
+//     plain loads.
 // Meanwhile the consumer warps turn the inputs into the fixed-point records
 // of kq_xrec.cuh in shared memory (or read them from global memory, where a
 // separate pass wrote them, when they do not fit).  Every consumer warp
@@ -59,8 +60,9 @@ struct StreamMember {
     // ng groups of gq or gq + 1 rows (the first gr one more)
     int32_t ng[2], gq[2], gr[2];
     int32_t rmax;   // rows per group at most
-    int32_t kb;     // blocks per box (Q4_K / Q5_K)
-    int32_t nmaps;  // tensor maps (box heights) for this member
+    int32_t kb;     // blocks per stage row
+    int32_t seg;    // Q6_K: bytes between row segments in a slot
+    int32_t nmaps;  // tensor maps (box heights) for this member (Q4_K / Q5_K)
     int32_t map_h[kMaxMaps];
 };
 
@@ -199,15 +201,8 @@ struct Groups {
     }
 };
 
-// Row pairs of a stage of h rows: rows p and p + hp for p < hp.  Q6_K rows
-// p and p + hp must start with the same 4-byte alignment, which holds when
-// hp * nb is even.
-template <bool Q6>
-__device__ __forceinline__ int pair_offset(int h, int nb) {
-    int hp = (h + 1) >> 1;
-    if (Q6 && (nb & 1) && (hp & 1) && h > 1) ++hp;
-    return hp;
-}
+// Row pairs of a stage of h rows: rows p and p + hp for p < hp.
+__device__ __forceinline__ int pair_offset(int h) { return (h + 1) >> 1; }
 
 // Rows of one task: a lane takes one block column of R rows of the stage,
 // p and p + hp, which share their inputs.
@@ -228,6 +223,7 @@ struct ConsumerCtx {
     int nslot, slot_bytes;
     int nb, kb, nbox, nstage;
     int64_t rows, row_bytes;
+    int q6_seg;
     float *y;
     Groups G;
     int *abort_flag;
@@ -260,12 +256,12 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
     int slot = 0, lap = 0, g = 0, k = 0;
     int64_t g0 = c.G.start(0), g1 = c.G.start(1);
     int h = (int)(g1 - g0);
-    int hp = R == 2 ? pair_offset<Q6>(h, nb) : h;
+    int hp = R == 2 ? pair_offset(h) : h;
     uint32_t hinv = c.hinv[hp];
 #pragma unroll 1
     for (int s = 0; s < c.nstage; ++s) {
-        const int b0 = Q6 ? 0 : k * c.kb;
-        const int kbv = Q6 ? nb : (nb - b0 < c.kb ? nb - b0 : c.kb);
+        const int b0 = k * c.kb;
+        const int kbv = nb - b0 < c.kb ? nb - b0 : c.kb;
         const int tasks = hp * kbv;
         const int nbat = (int)(((uint32_t)tasks + 31u) >> 5);
         const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
@@ -282,8 +278,6 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             ok = false;
         }
         if (ok) {
-            // byte offset of the group's first row inside the slot (Q6_K)
-            const uint32_t q6off = Q6 ? (uint32_t)((g0 * c.row_bytes) & 15) : 0u;
             // this warp's first batch: the one dealt to it in the rotation
             int dw = warp - rot;
             if (dw < 0) dw += kStreamConsumers;
@@ -309,10 +303,16 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                     if (R == 2) B[R - 1].p = reinterpret_cast<const uint4 *>(sdp + (r2 * c.kb + j) * BB);
                     block_q45<NTOK, Q5, R>(B, xr, part);
                 } else {
-                    // both rows' blocks share one alignment; one code path
-                    // for every lane, whatever its block's alignment
-                    const uint8_t *a0 = sdp + q6off + (r * nb + j) * 210;
-                    const uint8_t *a1 = sdp + q6off + (r2 * nb + j) * 210;
+                    // one code path for every lane, whatever its blocks'
+                    // alignment: row r's segment starts as far past a
+                    // 16-byte boundary as its first block does in memory
+                    // block start (row g0 + r, block b0) mod 16: the low four
+                    // bits survive 32-bit wrap-around
+                    const uint32_t base = (uint32_t)g0 * (uint32_t)c.row_bytes + (uint32_t)b0 * 210u;
+                    const uint32_t m0 = (base + (uint32_t)r * (uint32_t)c.row_bytes) & 15u;
+                    const uint32_t m1 = (base + (uint32_t)r2 * (uint32_t)c.row_bytes) & 15u;
+                    const uint8_t *a0 = sdp + r * c.q6_seg + m0 + j * 210;
+                    const uint8_t *a1 = sdp + r2 * c.q6_seg + m1 + j * 210;
                     Q6WordsShared W[R];
                     W[0] = Q6WordsShared::at(a0);
                     if (R == 2) W[R - 1] = Q6WordsShared::at(a1);
@@ -372,7 +372,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             g0 = g1;
             g1 = c.G.start(g + 1);
             h = (int)(g1 - g0);
-            hp = h < 1 ? 1 : (R == 2 ? pair_offset<Q6>(h, nb) : h);
+            hp = h < 1 ? 1 : (R == 2 ? pair_offset(h) : h);
             hinv = c.hinv[hp];
         }
     }
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     Groups G;
     G.init(cidx, M);
     const bool q6 = fmt == kFmtQ6K;
-    const int nbox = q6 ? 1 : (nb + M.kb - 1) / M.kb;
+    const int nbox = (nb + M.kb - 1) / M.kb;
     const int nstage = G.ng * nbox;
     const int nslot = p.nslot;
 
@@ -427,7 +427,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     if (warp == kStreamConsumers) {
         // ------------------------------------------------ producer
-        if (lane != 0) return;
+        // Lane 0 takes every decision and every wait and shares the outcome
+        // with the warp; the other lanes only help issue Q6_K row-segment
+        // copies (lane r copies rows r, r + 32, ...).
+        constexpr unsigned kAll = 0xFFFFFFFFu;
         // The consumers' input loads must not queue behind the weight
         // stream.  The producer issues `gate` stages, then waits until every
         // consumer warp is about to issue its input loads (a relaxed
@@ -436,15 +439,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // consumers still wait for the preceding kernel.
         const int gate = XSMEM ? (p.overlap ? kOverlapPrefetch : 0) : -1;
         auto wait_inputs_issued = [&]() {
-            const unsigned long long t0 = global_ns();
-            while (*(volatile int *)&xissued < kStreamConsumers) {
-                __nanosleep(20);
-                if (global_ns() - t0 > kWaitLimitNs) {
-                    atomicExch(&abort_flag, 1);
-                    atomicOr(p.err, 1u);
-                    break;
+            if (lane == 0) {
+                const unsigned long long t0 = global_ns();
+                while (*(volatile int *)&xissued < kStreamConsumers) {
+                    __nanosleep(20);
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        atomicExch(&abort_flag, 1);
+                        atomicOr(p.err, 1u);
+                        break;
+                    }
                 }
             }
+            __syncwarp();
         };
         if (gate == 0) wait_inputs_issued();
         int issued = 0;
@@ -452,37 +458,62 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         int64_t g0 = G.start(0), g1 = G.start(1);
         for (int s = 0; s < nstage; ++s) {
             if (s == gate && s > 0) wait_inputs_issued();
-            if (*(volatile int *)&abort_flag) break;
-            if (s >= nslot) {
-                if (!mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1)) {
+            int stop = 0;
+            if (lane == 0) {
+                stop = *(volatile int *)&abort_flag;
+                if (!stop && s >= nslot && !mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1)) {
                     atomicExch(&abort_flag, 1);
                     atomicOr(p.err, 1u);
-                    break;
+                    stop = 1;
                 }
             }
+            if (__shfl_sync(kAll, stop, 0)) break;
             const int h = (int)(g1 - g0);
             const uint32_t dst = ring + (uint32_t)slot * p.slot_bytes;
             const uint32_t full = bars + 8 * slot;
             if (!q6) {
-                int mj = 0;
-                for (int j = 0; j < M.nmaps; ++j)
-                    if (M.map_h[j] == h) mj = j;
-                const int box_row = M.kb * bb;
-                mbar_expect_tx(full, (uint32_t)(h * box_row));
-                tensor2d_g2s(dst, &p.maps[mi][mj], k * (box_row / 8), (int)g0, full);
+                if (lane == 0) {
+                    int mj = 0;
+                    for (int j = 0; j < M.nmaps; ++j)
+                        if (M.map_h[j] == h) mj = j;
+                    const int box_row = M.kb * bb;
+                    mbar_expect_tx(full, (uint32_t)(h * box_row));
+                    tensor2d_g2s(dst, &p.maps[mi][mj], k * (box_row / 8), (int)g0, full);
+                }
             } else {
+                // one 16-byte-aligned bulk copy per row segment (blocks
+                // b0..b0+kbv of the row), segments M.seg bytes apart; the
+                // sub-16-byte tail at the very end of the matrix is copied
+                // with plain loads
                 const int64_t total = M.rows * row_bytes;
-                const int64_t A = g0 * row_bytes, B = g1 * row_bytes;
-                const int64_t A16 = A & ~(int64_t)15;
-                int64_t B16 = (B + 15) & ~(int64_t)15;
-                if (B16 > total) B16 = total & ~(int64_t)15;
-                // sub-16-byte tail at the very end of the matrix
+                const int b0 = k * M.kb;
+                const int kbv = nb - b0 < M.kb ? nb - b0 : M.kb;
                 uint8_t *dstp = smem + (dst - bars);
-                for (int64_t i = B16; i < B; ++i) dstp[i - A16] = M.W[i];
-                mbar_expect_tx(full, (uint32_t)(B16 - A16));
-                for (int64_t o = A16; o < B16; o += 32768) {
-                    const int64_t len = (B16 - o) < 32768 ? (B16 - o) : 32768;
-                    bulk_g2s(dst + (uint32_t)(o - A16), M.W + o, (uint32_t)len, full);
+                uint32_t tx = 0;
+                for (int r = lane; r < h; r += 32) {
+                    const int64_t a = (g0 + r) * row_bytes + (int64_t)b0 * 210;
+                    const int64_t e = a + (int64_t)kbv * 210;
+                    const int64_t a16 = a & ~(int64_t)15;
+                    int64_t e16 = (e + 15) & ~(int64_t)15;
+                    if (e16 > total) {
+                        e16 = total & ~(int64_t)15;
+                        for (int64_t i = e16; i < e; ++i) dstp[r * M.seg + (i - a16)] = M.W[i];
+                    }
+                    tx += (uint32_t)(e16 - a16);
+                }
+                tx = __reduce_add_sync(kAll, tx);
+                // the tail's plain stores are ordered before lane 0's
+                // arrive (a release) by the warp barrier
+                __syncwarp();
+                if (lane == 0) mbar_expect_tx(full, tx);
+                __syncwarp();
+                for (int r = lane; r < h; r += 32) {
+                    const int64_t a = (g0 + r) * row_bytes + (int64_t)b0 * 210;
+                    const int64_t e = a + (int64_t)kbv * 210;
+                    const int64_t a16 = a & ~(int64_t)15;
+                    int64_t e16 = (e + 15) & ~(int64_t)15;
+                    if (e16 > total) e16 = total & ~(int64_t)15;
+                    bulk_g2s(dst + (uint32_t)(r * M.seg), M.W + a16, (uint32_t)(e16 - a16), full);
                 }
             }
             issued = s + 1;
@@ -497,7 +528,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 g1 = G.start(g + 1);
             }
         }
-        if (*(volatile int *)&abort_flag) {
+        __syncwarp();
+        if (lane == 0 && *(volatile int *)&abort_flag) {
             // do not leave copies in flight into this CTA's shared memory
             for (int slot = 0; slot < nslot && slot < issued; ++slot) {
                 const int last = slot + ((issued - 1 - slot) / nslot) * nslot;
@@ -530,6 +562,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.nstage = nstage;
     c.rows = M.rows;
     c.row_bytes = row_bytes;
+    c.q6_seg = M.seg;
     c.y = M.y;
     c.G = G;
     c.abort_flag = &abort_flag;
