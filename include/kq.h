@@ -13,19 +13,27 @@
  *     Q5_K  176 B / block   w = d*sc_j*(nibble | hbit<<4) - dmin*m_j  (6.4)
  *     Q6_K  210 B / block   w = d*sc_j*(code - 32), 16 int8 scales   (6.5)
  *
- * x and y are f32.  ntok (1..8) token columns share one read of W.
+ * x and y are f32.  Up to 8 token columns share one read of W; a call with
+ * ntok = 9..16 runs as two launches (token columns 0..7, then 8..ntok-1),
+ * the second reading W again.  A token column's result does not depend on
+ * ntok or on the other columns, so the split changes no result.
  *
  * Conventions for every entry point below
  *   - Pointers to W, x and y are DEVICE pointers (cudaMalloc / torch CUDA
  *     storage on the current device), owned by the caller.  The library
- *     never allocates, frees or synchronizes device memory, and keeps no
- *     pointer after a call returns.
+ *     keeps no pointer after a call returns and never synchronizes.  Its
+ *     one allocation is a stream-ordered temporary (cudaMallocAsync /
+ *     cudaFreeAsync on `stream`) for the input records of calls whose
+ *     records do not fit in shared memory; kq_matvec_noalloc allocates
+ *     nothing.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream) and may be captured in a CUDA graph.
  *   - Every argument is validated on the host before anything is launched;
- *     a call that returns an error has enqueued nothing.  KQ_ERR_CUDA means
- *     the launch itself failed; kq_last_cuda_error() returns the CUDA error
- *     code of the most recent such failure on the calling thread.
+ *     a call that returns an error has enqueued nothing, with one exception:
+ *     KQ_ERR_CUDA from the second launch of a call with ntok > 8, after the
+ *     first had been enqueued.  KQ_ERR_CUDA means a launch itself failed;
+ *     kq_last_cuda_error() returns the CUDA error code of the most recent
+ *     such failure on the calling thread.
  *   - Results are deterministic: a row's arithmetic depends only on the
  *     format, cols, ntok and that row's bytes and inputs -- not on the grid,
  *     the number of rows, or which other matrices share the launch.
@@ -61,7 +69,7 @@ typedef enum kq_status {
     KQ_ERR_LIMIT = 10   /* kq_matvec_noalloc: inputs beyond its fixed buffer  */
 } kq_status;
 
-#define KQ_MAX_NTOK 8
+#define KQ_MAX_NTOK 16
 #define KQ_MAX_SET 16
 /* Largest accepted cols (inputs per row). */
 #define KQ_MAX_COLS (1LL << 20)
@@ -213,6 +221,14 @@ int kq_set_overlap(int enable);
 int kq_last_kernels(void);
 
 /*
+ * Number of kernel launches the calling thread's most recent successful
+ * kq_matvec / kq_matvec_set / kq_matvec_noalloc call enqueued (the record
+ * pass counts as one; a call with ntok > 8 counts both of its launches).
+ * 0 before any call.
+ */
+int kq_last_launch_count(void);
+
+/*
  * kq_matvec without any memory allocation.  The pages have no counterpart:
  * this is a library service for callers that must not allocate device
  * memory during the call -- code running under a caller-managed memory
@@ -223,10 +239,12 @@ int kq_last_kernels(void);
  * Same arguments, result and errors as kq_matvec, computed by the direct-
  * load kernel with its input records (see the record pass) in one fixed
  * file-scope device buffer of KQ_NOALLOC_RECORD_BYTES bytes instead of a
- * stream-ordered temporary.  Calls whose records need more -- ntok * (cols
- * / 256) * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K -- return
- * KQ_ERR_LIMIT with nothing enqueued.  The records are written in full
- * before they are read, so nothing in the buffer has to start at zero.
+ * stream-ordered temporary.  Calls whose records need more -- min(ntok, 8)
+ * * (cols / 256) * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K (the
+ * records of one launch; ntok > 8 runs as two launches in stream order,
+ * one after the other in the buffer) -- return KQ_ERR_LIMIT with nothing
+ * enqueued.  The records are written in full before they are read, so
+ * nothing in the buffer has to start at zero.
  *
  * The first call on a device looks the buffer up (cudaGetSymbolAddress,
  * once per device); make that first call before any stream capture.  Every

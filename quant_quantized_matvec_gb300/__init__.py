@@ -17,7 +17,7 @@ from . import _binding
 
 Q4_K, Q5_K, Q6_K = 12, 13, 14
 FORMATS = (Q4_K, Q5_K, Q6_K)
-MAX_NTOK = 8
+MAX_NTOK = 16
 MAX_SET = 16
 
 
@@ -173,6 +173,11 @@ def last_kernels() -> dict:
     b = _lib().kq_last_kernels()
     return {"direct": bool(b & 1), "stream": bool(b & 2),
             "record_pass": bool(b & 4)}
+
+
+def last_launch_count() -> int:
+    """Kernel launches enqueued by this thread's last successful call."""
+    return int(_lib().kq_last_launch_count())
 
 
 def set_overlap(enable: bool) -> bool:

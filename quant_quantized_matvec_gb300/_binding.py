@@ -20,7 +20,7 @@ STATUS = {
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
            "kq_device_error", "kq_select_kernel", "kq_set_overlap",
-           "kq_last_kernels", "kq_matvec_noalloc", "kq_dequant_rows",
+           "kq_last_kernels", "kq_last_launch_count", "kq_matvec_noalloc", "kq_dequant_rows",
            "kq_version")
 
 
@@ -83,6 +83,8 @@ def load(path: str | None = None):
         lib.kq_set_overlap.restype = i32
         lib.kq_last_kernels.argtypes = []
         lib.kq_last_kernels.restype = i32
+        lib.kq_last_launch_count.argtypes = []
+        lib.kq_last_launch_count.restype = i32
         lib.kq_version.argtypes = []
         lib.kq_version.restype = i32
         if path is None:

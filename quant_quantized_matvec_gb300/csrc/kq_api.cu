@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(kPrepThreads) kq_xprep(const __grid_constant__
 namespace {
 
 thread_local int g_last_cuda_error = 0;
-thread_local int g_last_kernels = 0;  // kq_last_kernels
+thread_local int g_last_kernels = 0;   // kq_last_kernels
+thread_local int g_last_launches = 0;  // kq_last_launch_count
 
 int64_t block_bytes_of(int fmt) {
     switch (fmt) {
@@ -268,6 +269,7 @@ kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         return KQ_ERR_CUDA;
     }
     g_last_kernels = 1 | 4;
+    g_last_launches = 2;
     return KQ_OK;
 }
 
@@ -568,6 +570,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         return KQ_ERR_CUDA;
     }
     g_last_kernels = xsmem ? 2 : (2 | 4);
+    g_last_launches = xsmem ? 1 : 2;
     return KQ_OK;
 }
 
@@ -588,10 +591,43 @@ int kernel_choice() {
     return c;
 }
 
+// Token columns per launch.  A token's result depends on its own input
+// plane alone (every kernel treats the ntok columns independently), so a
+// call with more columns runs as launches of at most this many, with the
+// same results as one launch would give.
+constexpr int kLaunchNtok = 8;
+
+// The members of a set restricted to token columns [t0, t0 + nt).
+void token_chunk(const kq_mat *mats, int n, int t0, kq_mat *out) {
+    for (int i = 0; i < n; ++i) {
+        out[i] = mats[i];
+        out[i].x = mats[i].x + (int64_t)t0 * mats[i].cols;
+        out[i].y = mats[i].y + (int64_t)t0 * mats[i].rows;
+    }
+}
+
+kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream);
+
 kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
     const kq_status v = validate_set(mats, n, ntok);
     if (v != KQ_OK) return v;
+    if (ntok <= kLaunchNtok) return run_chunk(mats, n, ntok, stream);
+    kq_mat part[KQ_MAX_SET];
+    int kernels = 0, launches = 0;
+    for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {
+        token_chunk(mats, n, t0, part);
+        const kq_status st = run_chunk(part, n, std::min(kLaunchNtok, ntok - t0), stream);
+        if (st != KQ_OK) return st;
+        kernels |= g_last_kernels;
+        launches += g_last_launches;
+    }
+    g_last_kernels = kernels;
+    g_last_launches = launches;
+    return KQ_OK;
+}
 
+// One launch's worth (ntok <= kLaunchNtok) of a validated set.
+kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     DeviceInfo info;
@@ -631,13 +667,32 @@ cudaError_t noalloc_buffer(int dev, uint8_t **out) {
     return cudaSuccess;
 }
 
+kq_status run_noalloc_chunk(const kq_mat &m, int ntok, void *stream);
+
 kq_status run_noalloc(const kq_mat &m, int ntok, void *stream) {
     const kq_status v = validate_set(&m, 1, ntok);
     if (v != KQ_OK) return v;
+    // the records of one launch (at most kLaunchNtok tokens) must fit
     const int nb = (int)(m.cols / 256);
     const bool q6 = m.fmt == KQ_Q6_K;
-    const int64_t rec_total = (int64_t)ntok * nb * kq::rec_bytes(q6);
+    const int64_t rec_total = (int64_t)std::min(ntok, kLaunchNtok) * nb * kq::rec_bytes(q6);
     if (rec_total > KQ_NOALLOC_RECORD_BYTES) return KQ_ERR_LIMIT;
+    int launches = 0;
+    for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {
+        kq_mat part;
+        token_chunk(&m, 1, t0, &part);
+        // chunks run in stream order, so they reuse the one buffer in turn
+        const kq_status st = run_noalloc_chunk(part, std::min(kLaunchNtok, ntok - t0), stream);
+        if (st != KQ_OK) return st;
+        launches += g_last_launches;
+    }
+    g_last_launches = launches;
+    return KQ_OK;
+}
+
+kq_status run_noalloc_chunk(const kq_mat &m, int ntok, void *stream) {
+    const int nb = (int)(m.cols / 256);
+    const bool q6 = m.fmt == KQ_Q6_K;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -692,6 +747,7 @@ kq_status run_noalloc(const kq_mat &m, int ntok, void *stream) {
         return KQ_ERR_CUDA;
     }
     g_last_kernels = 1 | 4;
+    g_last_launches = 2;
     return KQ_OK;
 }
 
@@ -807,6 +863,7 @@ int kq_select_kernel(int which) {
 }
 
 int kq_last_kernels(void) { return g_last_kernels; }
+int kq_last_launch_count(void) { return g_last_launches; }
 
 int kq_set_overlap(int enable) {
     const int prev = g_overlap.load();
@@ -814,6 +871,6 @@ int kq_set_overlap(int enable) {
     return prev;
 }
 
-int kq_version(void) { return (1 << 16) | 1; }
+int kq_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"

@@ -66,7 +66,7 @@ def mv(lib, fmt=12, W=W0, rows=64, cols=512, x=X0, y=Y0, ntok=1):
     (dict(rows=0), SHAPE), (dict(rows=-3), SHAPE), (dict(cols=0), SHAPE),
     (dict(cols=255), SHAPE), (dict(cols=300), SHAPE),
     (dict(cols=1 << 21), SHAPE), (dict(rows=(1 << 30) + 1), SHAPE),
-    (dict(ntok=0), NTOK), (dict(ntok=9), NTOK), (dict(ntok=-1), NTOK),
+    (dict(ntok=0), NTOK), (dict(ntok=17), NTOK), (dict(ntok=-1), NTOK),
     (dict(W=None), NULL), (dict(x=None), NULL), (dict(y=None), NULL),
     (dict(W=W0 + 8), ALIGN), (dict(x=X0 + 4), ALIGN), (dict(y=Y0 + 2), ALIGN),
     # y overlapping W, or x
@@ -110,7 +110,7 @@ def test_set_rejects(lib):
     assert mvset(lib, [{}, {"fmt": 9}]) == FORMAT
     assert mvset(lib, [{}, {"cols": 100}]) == SHAPE
     assert mvset(lib, [{}, {"reserved": 1}]) == SHAPE
-    assert mvset(lib, [{}, {}], ntok=9) == NTOK
+    assert mvset(lib, [{}, {}], ntok=17) == NTOK
     assert mvset(lib, [{}, {"x": None}]) == NULL
     assert mvset(lib, [{}, {"W": W0 + 4}]) == ALIGN
     # two outputs overlapping each other

@@ -1,0 +1,113 @@
+"""ntok 9..16: the calls that run as two launches of at most 8 token
+columns.  Parity with the oracle, the split's invariant (a token column's
+output is the one a single-column call gives for it, bitwise), the set and
+the no-allocation entry point at these ntok."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import gpu_cases as C
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import quant_quantized_matvec_gb300 as kq  # noqa: E402
+from quant_quantized_matvec_gb300 import _binding  # noqa: E402
+
+FMTS = (kq.Q4_K, kq.Q5_K, kq.Q6_K)
+NAMES = {kq.Q4_K: "q4k", kq.Q5_K: "q5k", kq.Q6_K: "q6k"}
+
+
+def bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+@pytest.mark.parametrize("ntok", [9, 12, 16])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (77, 2816), (300, 768)])
+def test_small_ragged(fmt, ntok, rows, cols):
+    W, x = C.case(fmt, rows, cols, ntok, f"n16/{fmt}/{rows}/{cols}/{ntok}")
+    g = C.Guarded(ntok, rows)
+    kq.matvec(fmt, C.to_dev(W), rows, cols, C.to_dev(x), y=g.y)
+    torch.cuda.synchronize()
+    C.check(fmt, W, rows, cols, x, g.host(), what=f"{NAMES[fmt]} ntok={ntok}")
+    assert not kq.device_error()
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+def test_4096x6656_ntok16(fmt):
+    rows, cols, ntok = 4096, 6656, 16
+    W, x = C.case(fmt, rows, cols, ntok, f"n16/cfg/{fmt}")
+    g = C.Guarded(ntok, rows)
+    kq.matvec(fmt, C.to_dev(W), rows, cols, C.to_dev(x), y=g.y)
+    torch.cuda.synchronize()
+    C.check(fmt, W, rows, cols, x, g.host(), what=f"{NAMES[fmt]} 4096x6656 ntok=16")
+
+
+@pytest.mark.parametrize("kernel", ["stream", "direct"])
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+def test_token_columns_are_independent(fmt, kernel):
+    """Output column t of a 16-column call equals, bit for bit, the output
+    of a one-column call on x[t], for both kernels."""
+    rows, cols, ntok = 193, 3328, 16
+    W, x = C.case(fmt, rows, cols, ntok, f"n16/indep/{fmt}")
+    Wd = C.to_dev(W)
+    try:
+        kq.select_kernel(kernel)
+        g = C.Guarded(ntok, rows)
+        kq.matvec(fmt, Wd, rows, cols, C.to_dev(x), y=g.y)
+        singles = []
+        for t in (0, 5, 8, 11, 15):
+            s = C.Guarded(1, rows)
+            kq.matvec(fmt, Wd, rows, cols, C.to_dev(x[t:t + 1]), y=s.y)
+            singles.append((t, s))
+        torch.cuda.synchronize()
+    finally:
+        kq.select_kernel("auto")
+    y = g.host()
+    for t, s in singles:
+        assert np.array_equal(bits(y[t]), bits(s.host()[0])), f"column {t}"
+    assert not kq.device_error()
+
+
+def test_set_ntok16_equals_separate_calls():
+    """A concurrent set at ntok = 16 (Q4_K and Q6_K members sharing x)
+    writes what separate calls write."""
+    ntok, cols = 16, 2560
+    specs = [(kq.Q4_K, 640, "a"), (kq.Q6_K, 96, "b"), (kq.Q5_K, 257, "c")]
+    x = C.case(kq.Q4_K, 1, cols, ntok, "n16/set/x")[1]
+    xd = C.to_dev(x)
+    members, seps, hosts = [], [], []
+    for fmt, rows, tag in specs:
+        W = C.case(fmt, rows, cols, 1, f"n16/set/{tag}")[0]
+        Wd = C.to_dev(W)
+        gs, gp = C.Guarded(ntok, rows), C.Guarded(ntok, rows)
+        members.append((fmt, Wd, rows, cols, xd, gs.y))
+        kq.matvec(fmt, Wd, rows, cols, xd, y=gp.y)
+        seps.append((gs, gp))
+        hosts.append((fmt, W, rows))
+    kq.matvec_set(members)
+    torch.cuda.synchronize()
+    for (gs, gp), (fmt, W, rows) in zip(seps, hosts):
+        ys = gs.host()
+        assert np.array_equal(bits(ys), bits(gp.host()))
+        C.check(fmt, W, rows, cols, x, ys, what=f"set member {NAMES[fmt]}")
+    assert not kq.device_error()
+
+
+def test_noalloc_ntok12_equals_kq_matvec():
+    lib = _binding.load()
+    fmt, rows, cols, ntok = kq.Q6_K, 300, 6656, 12
+    W, x = C.case(fmt, rows, cols, ntok, "n16/noalloc")
+    Wd, xd = C.to_dev(W), C.to_dev(x)
+    a, b = C.Guarded(ntok, rows), C.Guarded(ntok, rows)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for fn, g in ((lib.kq_matvec_noalloc, a), (lib.kq_matvec, b)):
+        assert fn(fmt, ctypes.c_void_p(Wd.data_ptr()), rows, cols,
+                  ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(g.y.data_ptr()),
+                  ntok, stream) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(a.host()), bits(b.host()))
+    C.check(fmt, W, rows, cols, x, a.host(), what="noalloc ntok=12")
+    assert not kq.device_error()

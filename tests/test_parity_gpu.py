@@ -82,7 +82,7 @@ def test_rejects_without_launch():
     with pytest.raises(kq.KQError, match="KQ_ERR_ALIAS"):
         kq.matvec(fmt, Wd, rows, cols, xd, y=xd.view(-1)[:rows].view(1, rows))
     with pytest.raises(kq.KQError, match="KQ_ERR_NTOK"):
-        kq.matvec(fmt, Wd, rows, cols, C.to_dev(np.zeros((9, cols),
+        kq.matvec(fmt, Wd, rows, cols, C.to_dev(np.zeros((17, cols),
                                                           np.float32)))
 
 
