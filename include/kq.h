@@ -13,10 +13,12 @@
  *     Q5_K  176 B / block   w = d*sc_j*(nibble | hbit<<4) - dmin*m_j  (6.4)
  *     Q6_K  210 B / block   w = d*sc_j*(code - 32), 16 int8 scales   (6.5)
  *
- * x and y are f32.  Up to 8 token columns share one read of W; a call with
- * ntok = 9..16 runs as two launches (token columns 0..7, then 8..ntok-1),
- * the second reading W again.  A token column's result does not depend on
- * ntok or on the other columns, so the split changes no result.
+ * x and y are f32.  Up to 5 token columns share one read of W; a call with
+ * ntok = 6..16 runs as ceil(ntok / 5) launches over consecutive, near-equal
+ * runs of token columns (6 = 3 + 3, 8 = 4 + 4, 16 = 4 + 4 + 4 + 4), each
+ * reading W again -- faster than one launch, whose block sums grow with
+ * the columns.  A token column's result does not depend on ntok or on the
+ * other columns, so the split changes no result.
  *
  * Conventions for every entry point below
  *   - Pointers to W, x and y are DEVICE pointers (cudaMalloc / torch CUDA
@@ -30,8 +32,8 @@
  *     the legacy default stream) and may be captured in a CUDA graph.
  *   - Every argument is validated on the host before anything is launched;
  *     a call that returns an error has enqueued nothing, with one exception:
- *     KQ_ERR_CUDA from the second launch of a call with ntok > 8, after the
- *     first had been enqueued.  KQ_ERR_CUDA means a launch itself failed;
+ *     KQ_ERR_CUDA from a later launch of a call that runs as several
+ *     (ntok > 5), after the earlier ones had been enqueued.  KQ_ERR_CUDA means a launch itself failed;
  *     kq_last_cuda_error() returns the CUDA error code of the most recent
  *     such failure on the calling thread.
  *   - Results are deterministic: a row's arithmetic depends only on the
@@ -223,7 +225,8 @@ int kq_last_kernels(void);
 /*
  * Number of kernel launches the calling thread's most recent successful
  * kq_matvec / kq_matvec_set / kq_matvec_noalloc call enqueued (the record
- * pass counts as one; a call with ntok > 8 counts both of its launches).
+ * pass counts as one; a call that runs as several launches counts them
+ * all).
  * 0 before any call.
  */
 int kq_last_launch_count(void);

@@ -596,6 +596,26 @@ int kernel_choice() {
 // call with more columns runs as launches of at most this many, with the
 // same results as one launch would give.
 constexpr int kLaunchNtok = 8;
+// Token columns per launch of kq_matvec / kq_matvec_set, at most: a call
+// with more runs as ceil(ntok / limit) launches of near-equal size.  The
+// kernels' cost per token column is lowest at 3..5 columns (block sums
+// grow with the columns while the unrolled code and its registers grow
+// too); on GB300, 4096x6656 matrices, ntok = 8 took 29-39 us as 4 + 4 and
+// 40-50 us as one launch.  KQ_LAUNCH_NTOK=1..8 overrides the limit
+// (measurement only; the results are the same for every value).
+constexpr int kDefaultLaunchNtok = 5;
+std::atomic<int> g_launch_ntok{0};
+
+int launch_ntok() {
+    int c = g_launch_ntok.load();
+    if (c == 0) {
+        const char *e = getenv("KQ_LAUNCH_NTOK");
+        const int v = e ? atoi(e) : 0;
+        c = (v >= 1 && v <= kLaunchNtok) ? v : kDefaultLaunchNtok;
+        g_launch_ntok.store(c);
+    }
+    return c;
+}
 
 // The members of a set restricted to token columns [t0, t0 + nt).
 void token_chunk(const kq_mat *mats, int n, int t0, kq_mat *out) {
@@ -611,12 +631,17 @@ kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream);
 kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
     const kq_status v = validate_set(mats, n, ntok);
     if (v != KQ_OK) return v;
-    if (ntok <= kLaunchNtok) return run_chunk(mats, n, ntok, stream);
+    const int cn = launch_ntok();
+    if (ntok <= cn) return run_chunk(mats, n, ntok, stream);
+    // near-equal chunks: the first `rem` take one column more
+    const int nch = (ntok + cn - 1) / cn, base = ntok / nch, rem = ntok % nch;
     kq_mat part[KQ_MAX_SET];
     int kernels = 0, launches = 0;
-    for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {
+    for (int ci = 0, t0 = 0; ci < nch; ++ci) {
+        const int nt = base + (ci < rem ? 1 : 0);
         token_chunk(mats, n, t0, part);
-        const kq_status st = run_chunk(part, n, std::min(kLaunchNtok, ntok - t0), stream);
+        t0 += nt;
+        const kq_status st = run_chunk(part, n, nt, stream);
         if (st != KQ_OK) return st;
         kernels |= g_last_kernels;
         launches += g_last_launches;

@@ -1,4 +1,4 @@
-"""ntok 9..16: the calls that run as two launches of at most 8 token
+"""ntok 6..16: the calls that run as several launches of at most 5 token
 columns.  Parity with the oracle, the split's invariant (a token column's
 output is the one a single-column call gives for it, bitwise), the set and
 the no-allocation entry point at these ntok."""
