@@ -21,8 +21,14 @@
  * other columns, so the split changes no result.
  *
  * Conventions for every entry point below
- *   - Pointers to W, x and y are DEVICE pointers (cudaMalloc / torch CUDA
- *     storage on the current device), owned by the caller.  The library
+ *   - W is a DEVICE pointer (cudaMalloc / torch CUDA storage on the current
+ *     device).  x and y are device pointers too, or pointers into pinned
+ *     host memory (cudaHostAlloc, cudaHostRegister, torch pin_memory),
+ *     which the kernels read and write in place over the host link -- on
+ *     GB300 (Grace) that saves the separate copy of the outputs back to
+ *     the host.  Managed memory is accepted for x and y.  Anything else
+ *     (pageable host memory, another device's memory) is KQ_ERR_MEMORY.
+ *     All memory is owned by the caller.  The library
  *     keeps no pointer after a call returns and never synchronizes.  Its
  *     one allocation is a stream-ordered temporary (cudaMallocAsync /
  *     cudaFreeAsync on `stream`) for the input records of calls whose
@@ -68,7 +74,10 @@ typedef enum kq_status {
     KQ_ERR_COUNT = 7,   /* set size outside 1..KQ_MAX_SET                     */
     KQ_ERR_CUDA = 8,    /* the CUDA launch failed (see kq_last_cuda_error)    */
     KQ_ERR_TIMEOUT = 9, /* a bounded device-side wait expired                 */
-    KQ_ERR_LIMIT = 10   /* kq_matvec_noalloc: inputs beyond its fixed buffer  */
+    KQ_ERR_LIMIT = 10,  /* kq_matvec_noalloc: inputs beyond its fixed buffer  */
+    KQ_ERR_MEMORY = 11  /* W not in this device's memory, or x / y in memory
+                           the device cannot address (pageable host memory,
+                           another device's memory)                        */
 } kq_status;
 
 #define KQ_MAX_NTOK 16
@@ -101,15 +110,17 @@ int64_t kq_matrix_bytes(int fmt, int64_t rows, int64_t cols);
  *         super-blocks; 16-byte aligned.  Read only.
  *   rows  output rows, 1..KQ_MAX_ROWS.
  *   cols  inputs per row, a positive multiple of 256, at most KQ_MAX_COLS.
- *   x     device pointer, f32 [ntok][cols], contiguous, 16-byte aligned.
- *         Read only.
- *   y     device pointer, f32 [ntok][rows], contiguous, 4-byte aligned.
- *         Overwritten (not accumulated).  Must not overlap W or x.
+ *   x     device or pinned host pointer, f32 [ntok][cols], contiguous,
+ *         16-byte aligned.  Read only.
+ *   y     device or pinned host pointer, f32 [ntok][rows], contiguous,
+ *         4-byte aligned.  Overwritten (not accumulated).  Must not overlap
+ *         W or x.
  *   ntok  token columns, 1..KQ_MAX_NTOK.
  *   stream  cudaStream_t or NULL.
  *
- * Returns KQ_OK after enqueueing one kernel, or an error code with nothing
- * enqueued (KQ_ERR_CUDA: the launch was attempted and failed).
+ * Returns KQ_OK after enqueueing its kernel(s), or an error code (see the
+ * conventions above).  The pointers are checked with cudaPointerGetAttributes
+ * (KQ_ERR_MEMORY) after the host-only checks.
  */
 kq_status kq_matvec(int fmt, const void *W, int64_t rows, int64_t cols,
                     const float *x, float *y, int ntok, void *stream);

@@ -52,12 +52,15 @@ def _stream_ptr(stream) -> int:
     return int(stream.cuda_stream)
 
 
-def _check_tensor(t, name, dtype=None):
+def _check_tensor(t, name, dtype=None, host_ok=False):
+    """W must be a CUDA tensor; x and y (host_ok) may also be pinned CPU
+    tensors, which the kernels read and write in place."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor"
+                         + (" or a pinned CPU tensor" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -72,15 +75,16 @@ def matvec(fmt, W, rows, cols, x, y=None, stream=None):
     squeeze = x.dim() == 1
     x2 = x.unsqueeze(0) if squeeze else x
     _check_tensor(W, "W")
-    _check_tensor(x2, "x", torch.float32)
+    _check_tensor(x2, "x", torch.float32, host_ok=True)
     ntok = x2.shape[0]
     if x2.shape[1] != cols:
         raise ValueError("x must have cols columns")
     if W.numel() * W.element_size() != matrix_bytes(fmt, rows, cols):
         raise ValueError("W size does not match fmt/rows/cols")
     if y is None:
-        y = torch.empty((ntok, rows), dtype=torch.float32, device=x.device)
-    _check_tensor(y, "y", torch.float32)
+        y = torch.empty((ntok, rows), dtype=torch.float32,
+                        device=x.device if x.is_cuda else "cuda")
+    _check_tensor(y, "y", torch.float32, host_ok=True)
     if y.numel() != ntok * rows:
         raise ValueError("y must hold ntok*rows floats")
     st = _lib().kq_matvec(int(fmt), W.data_ptr(), int(rows), int(cols),
@@ -141,8 +145,8 @@ def matvec_set(members, ntok=None, stream=None, descriptors=None):
     if descriptors is None:
         for (fmt, W, rows, cols, x, y) in members:
             _check_tensor(W, "W")
-            _check_tensor(x, "x", torch.float32)
-            _check_tensor(y, "y", torch.float32)
+            _check_tensor(x, "x", torch.float32, host_ok=True)
+            _check_tensor(y, "y", torch.float32, host_ok=True)
             if x.numel() != ntok * cols or y.numel() != ntok * rows:
                 raise ValueError("x / y sizes do not match ntok, rows, cols")
             if W.numel() * W.element_size() != matrix_bytes(fmt, rows, cols):

@@ -15,7 +15,7 @@ STATUS = {
     0: "KQ_OK", 1: "KQ_ERR_FORMAT", 2: "KQ_ERR_SHAPE", 3: "KQ_ERR_NTOK",
     4: "KQ_ERR_NULL", 5: "KQ_ERR_ALIGN", 6: "KQ_ERR_ALIAS",
     7: "KQ_ERR_COUNT", 8: "KQ_ERR_CUDA", 9: "KQ_ERR_TIMEOUT",
-    10: "KQ_ERR_LIMIT",
+    10: "KQ_ERR_LIMIT", 11: "KQ_ERR_MEMORY",
 }
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
            "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",

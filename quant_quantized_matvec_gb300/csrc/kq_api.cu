@@ -151,6 +151,62 @@ kq_status validate_set(const kq_mat *mats, int n, int ntok) {
     return KQ_OK;
 }
 
+// ---------------------------------------------------------------- memory
+// Where each pointer may point: W into device memory of the current device
+// (the weight stream uses TMA); x and y into device memory of the current
+// device, managed memory, or host memory mapped into the device's address
+// space (pinned: cudaHostAlloc / cudaHostRegister), which the kernels read
+// and write in place over the host link.  `alias` is the address the device
+// uses.  A failed query is KQ_ERR_CUDA; anything else is KQ_ERR_MEMORY.
+kq_status device_address(const void *p, int dev, bool host_ok, const void **alias) {
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+        if (a.device != dev) return KQ_ERR_MEMORY;
+        *alias = p;
+        return KQ_OK;
+    case cudaMemoryTypeManaged:
+        *alias = p;
+        return KQ_OK;
+    case cudaMemoryTypeHost:
+        if (!host_ok || !a.devicePointer) return KQ_ERR_MEMORY;
+        *alias = a.devicePointer;
+        return KQ_OK;
+    default:
+        return KQ_ERR_MEMORY;
+    }
+}
+
+// The set with every pointer checked and replaced by its device address;
+// a pointer that repeats (a shared x) is looked up once.
+kq_status resolve_set(const kq_mat *mats, int n, int dev, kq_mat *out) {
+    for (int i = 0; i < n; ++i) {
+        out[i] = mats[i];
+        for (int k = 0; k < 3; ++k) {
+            const void *p = k == 0 ? mats[i].W : k == 1 ? (const void *)mats[i].x : (const void *)mats[i].y;
+            const void *q = nullptr;
+            for (int j = 0; j < i && !q; ++j) {
+                if (mats[j].W == p) q = out[j].W;
+                else if ((const void *)mats[j].x == p) q = out[j].x;
+                else if ((const void *)mats[j].y == p) q = out[j].y;
+            }
+            if (!q) {
+                const kq_status st = device_address(p, dev, k != 0, &q);
+                if (st != KQ_OK) return st;
+            }
+            if (k == 0) out[i].W = q;
+            else if (k == 1) out[i].x = static_cast<const float *>(q);
+            else out[i].y = static_cast<float *>(const_cast<void *>(q));
+        }
+    }
+    return KQ_OK;
+}
+
 // ---------------------------------------------------------------- device
 struct DeviceInfo {
     int sms = 0;
@@ -628,9 +684,18 @@ void token_chunk(const kq_mat *mats, int n, int t0, kq_mat *out) {
 
 kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream);
 
-kq_status run_set(const kq_mat *mats, int n, int ntok, void *stream) {
-    const kq_status v = validate_set(mats, n, ntok);
+kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
+    const kq_status v = validate_set(in, n, ntok);
     if (v != KQ_OK) return v;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    kq_mat mats[KQ_MAX_SET];
+    const kq_status r = resolve_set(in, n, dev, mats);
+    if (r != KQ_OK) return r;
     const int cn = launch_ntok();
     if (ntok <= cn) return run_chunk(mats, n, ntok, stream);
     // near-equal chunks: the first `rem` take one column more
@@ -694,14 +759,23 @@ cudaError_t noalloc_buffer(int dev, uint8_t **out) {
 
 kq_status run_noalloc_chunk(const kq_mat &m, int ntok, void *stream);
 
-kq_status run_noalloc(const kq_mat &m, int ntok, void *stream) {
-    const kq_status v = validate_set(&m, 1, ntok);
+kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
+    const kq_status v = validate_set(&in, 1, ntok);
     if (v != KQ_OK) return v;
     // the records of one launch (at most kLaunchNtok tokens) must fit
-    const int nb = (int)(m.cols / 256);
-    const bool q6 = m.fmt == KQ_Q6_K;
+    const int nb = (int)(in.cols / 256);
+    const bool q6 = in.fmt == KQ_Q6_K;
     const int64_t rec_total = (int64_t)std::min(ntok, kLaunchNtok) * nb * kq::rec_bytes(q6);
     if (rec_total > KQ_NOALLOC_RECORD_BYTES) return KQ_ERR_LIMIT;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    kq_mat m;
+    const kq_status r = resolve_set(&in, 1, dev, &m);
+    if (r != KQ_OK) return r;
     int launches = 0;
     for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {
         kq_mat part;
@@ -849,7 +923,7 @@ const char *kq_status_str(int status) {
     case KQ_OK: return "ok";
     case KQ_ERR_FORMAT: return "unknown block format";
     case KQ_ERR_SHAPE: return "invalid or unsupported rows/cols";
-    case KQ_ERR_NTOK: return "ntok outside 1..8";
+    case KQ_ERR_NTOK: return "ntok outside 1..16";
     case KQ_ERR_NULL: return "null pointer";
     case KQ_ERR_ALIGN: return "misaligned pointer (W, x: 16 bytes; y: 4 bytes)";
     case KQ_ERR_ALIAS: return "an output overlaps an input or another output";
@@ -857,6 +931,7 @@ const char *kq_status_str(int status) {
     case KQ_ERR_CUDA: return "CUDA launch failed";
     case KQ_ERR_TIMEOUT: return "device-side wait timed out";
     case KQ_ERR_LIMIT: return "inputs exceed the fixed buffer of kq_matvec_noalloc";
+    case KQ_ERR_MEMORY: return "a pointer addresses memory the device cannot use there";
     default: return "unknown status";
     }
 }
