@@ -272,6 +272,11 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             atomicOr(c.err, 1u);
             ok = false;
         }
+        // Every warp waits for the slot, even one dealt no batch of this
+        // stage: the wait keeps its arrival on the slot's empty barrier in
+        // the right lap (a warp that skipped it could arrive for the slot's
+        // next lap before this lap's readers are done, and the producer
+        // would overwrite the slot under them).
         if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1, 128)) {
             atomicExch(c.abort_flag, 1);
             atomicOr(c.err, 1u);
