@@ -1,0 +1,44 @@
+/*
+ * kq_internal.h -- introspection of libkq.so for its host tests.  Not part
+ * of the matvec path: no call here touches a GPU or launches anything.
+ */
+#ifndef KQ_INTERNAL_H
+#define KQ_INTERNAL_H
+
+#include <stdint.h>
+
+#include "kq.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
+ * KQ_PLAN_MEMBER per member. */
+#define KQ_PLAN_HEAD 10
+#define KQ_PLAN_MEMBER 20
+
+/*
+ * The streaming kernel's launch geometry for the set `mats` (n members,
+ * ntok 1..8 token columns in the launch) on a device with `sms` SMs and
+ * `smem_optin` bytes of opt-in shared memory per CTA, as the library would
+ * plan it.  Pure host arithmetic on the descriptors' shapes and formats
+ * (their pointers are not read).
+ *
+ * out (host, at least KQ_PLAN_HEAD + n * KQ_PLAN_MEMBER int64 entries):
+ *   [0] kq_status of the plan (KQ_ERR_SHAPE: the direct kernel would run)
+ *   [1] grid  [2] level (-1: records in global memory)  [3] records in
+ *   shared memory (0/1)  [4] x_bytes  [5] part_bytes  [6] slot_bytes
+ *   [7] nslot  [8] dynamic shared memory  [9] stages of the largest CTA
+ *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
+ *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes.
+ * Returns 0, or -1 for bad arguments (nothing written).
+ */
+int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
+                     int64_t *out, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_INTERNAL_H */

@@ -81,6 +81,8 @@ def load(path: str | None = None):
         lib.kq_select_kernel.restype = i32
         lib.kq_set_overlap.argtypes = [i32]
         lib.kq_set_overlap.restype = i32
+        lib.kq_plan_describe.argtypes = [vp, i32, i32, i32, i32, vp, i32]
+        lib.kq_plan_describe.restype = i32
         lib.kq_last_kernels.argtypes = []
         lib.kq_last_kernels.restype = i32
         lib.kq_last_launch_count.argtypes = []

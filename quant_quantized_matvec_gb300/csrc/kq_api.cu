@@ -14,6 +14,7 @@
 
 #include "kq.h"
 #include "kq_launch.cuh"
+#include "kq_plan.h"
 
 KQ_DECLARE_INSTANCES(1)
 KQ_DECLARE_INSTANCES(2)
@@ -402,12 +403,6 @@ bool tensor_map(const void *W, int64_t rows, int64_t row_bytes, int box_w, int b
     return true;
 }
 
-int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
-
-// Consumer cost per weight byte of Q6_K relative to Q4_K, in sixteenths
-// (measured: the Q6_K block loop spends more instructions per byte).
-constexpr int64_t kCostQ6 = 32;
-
 // Launch overlap with the preceding kernel (kq_set_overlap).
 std::atomic<int> g_overlap{0};
 
@@ -421,192 +416,56 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     std::lock_guard<std::mutex> plock(pmu);
     memset(&p, 0, sizeof(p));
     p.n = n;
-    const int G = info.sms;
 
-    // CTAs per member in proportion to its work (at least one, at most one
-    // per row), largest remainder first.  Work is bytes weighted by the
-    // format's consumer cost per byte relative to Q4_K (kCostQ6 / 16 for
-    // Q6_K, whose blocks take more instructions per byte).
-    int64_t bytes[KQ_MAX_SET], total = 0;
+    // launch geometry (kq_plan.cu)
+    kqplan::Plan P;
+    const kq_status ps = kqplan::plan_stream(mats, n, ntok, info.sms, info.smem_optin, &P);
+    if (ps != KQ_OK) return ps;
     for (int i = 0; i < n; ++i) {
-        bytes[i] = mats[i].rows * (mats[i].cols / 256) * block_bytes_of(mats[i].fmt);
-        if (mats[i].fmt == KQ_Q6_K) bytes[i] = bytes[i] * kCostQ6 / 16;
-        total += bytes[i];
-    }
-    int ncta[KQ_MAX_SET];
-    double rem[KQ_MAX_SET];
-    int used = 0;
-    for (int i = 0; i < n; ++i) {
-        const double share = (double)G * (double)bytes[i] / (double)total;
-        ncta[i] = std::max(1, (int)share);
-        rem[i] = share - (int)share;
-        ncta[i] = (int)std::min<int64_t>(ncta[i], mats[i].rows);
-        used += ncta[i];
-    }
-    while (used < G) {
-        int best = -1;
-        for (int i = 0; i < n; ++i)
-            if (ncta[i] < mats[i].rows && (best < 0 || rem[i] > rem[best])) best = i;
-        if (best < 0) break;
-        ++ncta[best];
-        rem[best] = -1.0;
-        ++used;
-    }
-    while (used > G) {  // only when n > G
-        int best = 0;
-        for (int i = 1; i < n; ++i)
-            if (ncta[i] > ncta[best]) best = i;
-        if (ncta[best] <= 1) break;
-        --ncta[best];
-        --used;
-    }
-
-    // Stage geometry, from the largest stages down ("levels"): stages are
-    // [h rows][kb blocks] with h <= rcap and stage rows of at most kb_bytes
-    // (Q6_K row segments sit seg bytes apart in the slot, seg = 16 * odd so
-    // that rows start on different bank groups, with room for the segment's
-    // misalignment at both ends).  The first level whose input records fit
-    // in shared memory beside at least three slots (two at the smallest
-    // level, or when a CTA has only two stages) is taken; if none fits,
-    // level 0 with the records in global memory.
-    static const int kLevelRcap[] = {32, 16, 16, 8, 8};
-    static const int kLevelKbBytes[] = {2048, 2048, 1024, 1024, 512};
-    constexpr int kLevels = 5;
-    // the 1 KiB alignment of the dynamic region pads the static part to 1 KiB
-    const int64_t budget = (int64_t)info.smem_optin - 1024;
-    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0, nslot = 0, stages = 0;
-    int cta = 0;
-    bool xsmem = false;
-    auto plan = [&](int level) -> kq_status {
-        const int rcap = kLevelRcap[level], kb_bytes = kLevelKbBytes[level];
-        x_bytes = part_bytes = slot_bytes = stages = 0;
-        cta = 0;
-        for (int i = 0; i < n; ++i) {
-            const kq_mat &m = mats[i];
-            kq::StreamMember &M = p.m[i];
-            const int nb = (int)(m.cols / 256);
-            const int bb = (int)block_bytes_of(m.fmt);
-            const int64_t row_bytes = (int64_t)nb * bb;
-            M.W = (const uint8_t *)m.W;
-            M.x = m.x;
-            M.rec = nullptr;
-            M.y = m.y;
-            M.rows = m.rows;
-            M.nb = nb;
-            M.fmt = m.fmt;
-            M.cta_begin = cta;
-            M.ncta = ncta[i];
-            M.rows_q = (int32_t)(m.rows / ncta[i]);
-            M.rows_r = (int32_t)(m.rows % ncta[i]);
-            cta += ncta[i];
-            // rows per group: partials for the group must fit in 64 KiB
-            const int64_t part_row = (int64_t)nb * ntok * 4;
-            const int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
-            if (rmax < 1) return KQ_ERR_SHAPE;
-            M.rmax = rmax;
-            for (int big = 0; big < 2; ++big) {  // CTAs of rows_q / rows_q + 1 rows
-                const int64_t nn = M.rows_q + big;
-                const int64_t ng = nn > 0 ? (nn + rmax - 1) / rmax : 1;
-                M.ng[big] = (int32_t)ng;
-                M.gq[big] = (int32_t)(nn / ng);
-                M.gr[big] = (int32_t)(nn % ng);
-            }
-            // Blocks per box: a box row is at most kb_bytes (and 256 u64);
-            // prefer few boxes per row, then no zero-filled tail, then an odd
-            // number of 16-byte units per row (rows on distinct banks).
-            {
-                const int kbmax = (int)std::max<int64_t>(1, std::min<int64_t>(nb, kb_bytes / bb));
-                int best = 1;
-                int64_t best_key = INT64_MAX;
-                for (int kb = 1; kb <= kbmax; ++kb) {
-                    const int64_t nbox = (nb + kb - 1) / kb, waste = nbox * kb - nb;
-                    const int64_t units = (int64_t)kb * bb / 16;
-                    const int64_t key = nbox * 1000000 + waste * 10 + ((units & 1) ? 0 : 1);
-                    if (key < best_key) {
-                        best_key = key;
-                        best = kb;
-                    }
-                }
-                M.kb = best;
-            }
-            // group heights that occur: n in {floor, ceil}(rows / ncta)
-            int hs[kq::kMaxMaps], nh = 0, hmax = 0;
-            const int64_t nlo = m.rows / ncta[i], nhi = (m.rows + ncta[i] - 1) / ncta[i];
-            for (int64_t nn = nlo; nn <= nhi; ++nn) {
-                if (nn < 1) continue;
-                const int64_t ng = (nn + rmax - 1) / rmax;
-                for (int64_t hh = nn / ng; hh <= (nn + ng - 1) / ng; ++hh) {
-                    bool seen = false;
-                    for (int j = 0; j < nh; ++j) seen |= hs[j] == hh;
-                    if (!seen) {
-                        if (nh == kq::kMaxMaps) return KQ_ERR_SHAPE;
-                        hs[nh++] = (int)hh;
-                    }
-                    hmax = std::max<int>(hmax, (int)hh);
-                }
-            }
-            // tasks of a stage (row pairs x block columns) stay below 2^12, the
-            // range of the kernel's multiply-shift division
-            {
-                const int hp = kq::stream_rows_per_task(m.fmt, ntok) == 2 ? (hmax + 1) / 2 : hmax;
-                if ((int64_t)hp * M.kb >= 4096) return KQ_ERR_SHAPE;
-            }
-            M.nmaps = m.fmt == KQ_Q6_K ? 0 : nh;
-            M.seg = 0;
-            if (m.fmt != KQ_Q6_K) {
-                const int box_w = (int)(M.kb * bb / 8);
-                for (int j = 0; j < nh; ++j) {
-                    M.map_h[j] = hs[j];
-                    if (!tensor_map(m.W, m.rows, row_bytes, box_w, hs[j], &p.maps[i][j]))
-                        return KQ_ERR_SHAPE;
-                }
-                slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * M.kb * bb);
-            } else {
-                // a segment of kb blocks starts up to 14 bytes past a 16-byte
-                // boundary and its copy ends up to 14 bytes past its end
-                int seg = (int)round_up((int64_t)M.kb * 210 + 28, 16);
-                if (((seg / 16) & 1) == 0) seg += 16;
-                M.seg = seg;
-                slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)hmax * seg);
-            }
-            // stages of this member's largest CTA
-            stages = std::max<int64_t>(stages, (int64_t)M.ng[M.rows_r > 0 ? 1 : 0] *
-                                                   ((nb + M.kb - 1) / M.kb));
-            // input records [ntok][nb] (kq_xrec.cuh)
-            x_bytes = std::max<int64_t>(x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
-            part_bytes = std::max<int64_t>(part_bytes, (int64_t)hmax * part_row);
+        const kq_mat &m = mats[i];
+        const kqplan::Member &Q = P.m[i];
+        kq::StreamMember &M = p.m[i];
+        M.W = (const uint8_t *)m.W;
+        M.x = m.x;
+        M.rec = nullptr;
+        M.y = m.y;
+        M.rows = m.rows;
+        M.nb = (int)(m.cols / 256);
+        M.fmt = m.fmt;
+        M.cta_begin = Q.cta_begin;
+        M.ncta = Q.ncta;
+        M.rows_q = Q.rows_q;
+        M.rows_r = Q.rows_r;
+        for (int big = 0; big < 2; ++big) {
+            M.ng[big] = Q.ng[big];
+            M.gq[big] = Q.gq[big];
+            M.gr[big] = Q.gr[big];
         }
-        part_bytes = 2 * round_up(part_bytes, 128);  // two row groups in flight
-        slot_bytes = round_up(slot_bytes, 128);
-        x_bytes = round_up(x_bytes, 128);
-        return KQ_OK;
-    };
-    int level = -1;
-    for (int L = 0; L < kLevels && level < 0; ++L) {
-        if (plan(L) != KQ_OK) continue;
-        const int64_t slots = (budget - 1024 - x_bytes - part_bytes) / slot_bytes;
-        const int64_t want = std::min<int64_t>(L == kLevels - 1 ? 2 : 3, std::max<int64_t>(2, stages));
-        if (slots >= want) level = L;
+        M.rmax = Q.rmax;
+        M.kb = Q.kb;
+        M.seg = Q.seg;
+        M.nmaps = m.fmt == KQ_Q6_K ? 0 : Q.nh;
+        if (m.fmt != KQ_Q6_K) {
+            // one tensor map per group height: boxes [h][kb * BB / 8] of u64
+            const int box_w = (int)(Q.kb * block_bytes_of(m.fmt) / 8);
+            for (int j = 0; j < Q.nh; ++j) {
+                M.map_h[j] = Q.hs[j];
+                if (!tensor_map(m.W, m.rows, Q.row_bytes, box_w, Q.hs[j], &p.maps[i][j]))
+                    return KQ_ERR_SHAPE;
+            }
+        }
     }
-    if (level >= 0) {
-        xsmem = true;
-    } else {
-        const kq_status ps = plan(0);
-        if (ps != KQ_OK) return ps;
-        x_bytes = 0;
-    }
-    const int64_t fixed = 1024 + x_bytes + part_bytes;
-    nslot = std::min<int64_t>(kq::kMaxSlots, (budget - fixed) / slot_bytes);
-    if (nslot < 2) return KQ_ERR_SHAPE;
-    p.nslot = (int)nslot;
-    p.slot_bytes = (int)slot_bytes;
-    p.x_bytes = (int)x_bytes;
-    p.part_bytes = (int)part_bytes;
+    const bool xsmem = P.xsmem;
+    const int cta = P.grid;
+    p.nslot = (int)P.nslot;
+    p.slot_bytes = (int)P.slot_bytes;
+    p.x_bytes = (int)P.x_bytes;
+    p.part_bytes = (int)P.part_bytes;
     p.overlap = g_overlap.load() ? 1 : 0;
     for (int hp = 1; hp <= kq::kMaxHinv; ++hp) p.hinv[hp] = ((1u << 20) + hp - 1) / hp;
     p.hinv[0] = 1u << 20;
     p.err = info.err;
-    const size_t smem = (size_t)(fixed + nslot * slot_bytes);
+    const size_t smem = (size_t)P.smem;
     *launched = true;
     GlobalRecords gr;
     cudaError_t e = cudaSuccess;

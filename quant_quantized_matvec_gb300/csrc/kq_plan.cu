@@ -1,0 +1,219 @@
+// kq_plan.cu -- launch geometry of the streaming kernel (host only).
+#include "kq_plan.h"
+
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "kq_internal.h"
+#include "kq_kernel_stream.cuh"
+#include "kq_xrec.cuh"
+
+namespace kqplan {
+
+namespace {
+
+int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+int64_t block_bytes(int fmt) { return fmt == KQ_Q4_K ? 144 : fmt == KQ_Q5_K ? 176 : 210; }
+
+// CTAs per member in proportion to its work (at least one, at most one per
+// row), largest remainder first.  Work is bytes weighted by the format's
+// consumer cost per byte relative to Q4_K.
+void split_ctas(const kq_mat *mats, int n, int G, int *ncta) {
+    int64_t bytes[KQ_MAX_SET], total = 0;
+    for (int i = 0; i < n; ++i) {
+        bytes[i] = mats[i].rows * (mats[i].cols / 256) * block_bytes(mats[i].fmt);
+        if (mats[i].fmt == KQ_Q6_K) bytes[i] = bytes[i] * kCostQ6 / 16;
+        total += bytes[i];
+    }
+    double rem[KQ_MAX_SET];
+    int used = 0;
+    for (int i = 0; i < n; ++i) {
+        const double share = (double)G * (double)bytes[i] / (double)total;
+        ncta[i] = std::max(1, (int)share);
+        rem[i] = share - (int)share;
+        ncta[i] = (int)std::min<int64_t>(ncta[i], mats[i].rows);
+        used += ncta[i];
+    }
+    while (used < G) {
+        int best = -1;
+        for (int i = 0; i < n; ++i)
+            if (ncta[i] < mats[i].rows && (best < 0 || rem[i] > rem[best])) best = i;
+        if (best < 0) break;
+        ++ncta[best];
+        rem[best] = -1.0;
+        ++used;
+    }
+    while (used > G) {  // only when n > G
+        int best = 0;
+        for (int i = 1; i < n; ++i)
+            if (ncta[i] > ncta[best]) best = i;
+        if (ncta[best] <= 1) break;
+        --ncta[best];
+        --used;
+    }
+}
+
+// Stage geometry levels, from the largest stages down: stages are
+// [h rows][kb blocks] with h <= rcap and stage rows of at most kb_bytes.
+constexpr int kLevelRcap[] = {32, 16, 16, 8, 8};
+constexpr int kLevelKbBytes[] = {2048, 2048, 1024, 1024, 512};
+constexpr int kLevels = 5;
+
+// The geometry of one level (x_bytes: records in shared memory).
+kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int level, Plan &P) {
+    const int rcap = kLevelRcap[level], kb_bytes = kLevelKbBytes[level];
+    P.x_bytes = P.part_bytes = P.slot_bytes = P.stages = 0;
+    int cta = 0;
+    for (int i = 0; i < n; ++i) {
+        const kq_mat &m = mats[i];
+        Member &M = P.m[i];
+        M = Member{};
+        const int nb = (int)(m.cols / 256);
+        const int bb = (int)block_bytes(m.fmt);
+        M.row_bytes = (int64_t)nb * bb;
+        M.cta_begin = cta;
+        M.ncta = ncta[i];
+        M.rows_q = (int)(m.rows / ncta[i]);
+        M.rows_r = (int)(m.rows % ncta[i]);
+        cta += ncta[i];
+        // rows per group: partials for the group must fit in 64 KiB
+        const int64_t part_row = (int64_t)nb * ntok * 4;
+        const int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
+        if (rmax < 1) return KQ_ERR_SHAPE;
+        M.rmax = rmax;
+        for (int big = 0; big < 2; ++big) {  // CTAs of rows_q / rows_q + 1 rows
+            const int64_t nn = M.rows_q + big;
+            const int64_t ng = nn > 0 ? (nn + rmax - 1) / rmax : 1;
+            M.ng[big] = (int)ng;
+            M.gq[big] = (int)(nn / ng);
+            M.gr[big] = (int)(nn % ng);
+        }
+        // Blocks per stage row: at most kb_bytes (and 256 u64); prefer few
+        // stages per row, then no zero-filled tail, then an odd number of
+        // 16-byte units per row (rows on distinct banks).
+        {
+            const int kbmax = (int)std::max<int64_t>(1, std::min<int64_t>(nb, kb_bytes / bb));
+            int best = 1;
+            int64_t best_key = INT64_MAX;
+            for (int kb = 1; kb <= kbmax; ++kb) {
+                const int64_t nbox = (nb + kb - 1) / kb, waste = nbox * kb - nb;
+                const int64_t units = (int64_t)kb * bb / 16;
+                const int64_t key = nbox * 1000000 + waste * 10 + ((units & 1) ? 0 : 1);
+                if (key < best_key) {
+                    best_key = key;
+                    best = kb;
+                }
+            }
+            M.kb = best;
+        }
+        // group heights that occur: n in {floor, ceil}(rows / ncta)
+        const int64_t nlo = m.rows / ncta[i], nhi = (m.rows + ncta[i] - 1) / ncta[i];
+        for (int64_t nn = nlo; nn <= nhi; ++nn) {
+            if (nn < 1) continue;
+            const int64_t ng = (nn + rmax - 1) / rmax;
+            for (int64_t hh = nn / ng; hh <= (nn + ng - 1) / ng; ++hh) {
+                bool seen = false;
+                for (int j = 0; j < M.nh; ++j) seen |= M.hs[j] == hh;
+                if (!seen) {
+                    if (M.nh == kMaxHeights) return KQ_ERR_SHAPE;
+                    M.hs[M.nh++] = (int)hh;
+                }
+                M.hmax = std::max<int>(M.hmax, (int)hh);
+            }
+        }
+        // tasks of a stage (row pairs x block columns) stay below 2^12, the
+        // range of the kernel's multiply-shift division
+        {
+            const int hp = kq::stream_rows_per_task(m.fmt, ntok) == 2 ? (M.hmax + 1) / 2 : M.hmax;
+            if ((int64_t)hp * M.kb >= 4096) return KQ_ERR_SHAPE;
+        }
+        if (m.fmt != KQ_Q6_K) {
+            P.slot_bytes = std::max<int64_t>(P.slot_bytes, (int64_t)M.hmax * M.kb * bb);
+        } else {
+            // a segment of kb blocks starts up to 14 bytes past a 16-byte
+            // boundary and its copy ends up to 14 bytes past its end
+            int seg = (int)round_up((int64_t)M.kb * 210 + 28, 16);
+            if (((seg / 16) & 1) == 0) seg += 16;
+            M.seg = seg;
+            P.slot_bytes = std::max<int64_t>(P.slot_bytes, (int64_t)M.hmax * seg);
+        }
+        // stages of this member's largest CTA
+        P.stages = std::max<int64_t>(P.stages, (int64_t)M.ng[M.rows_r > 0 ? 1 : 0] *
+                                                   ((nb + M.kb - 1) / M.kb));
+        // input records [ntok][nb] (kq_xrec.cuh)
+        P.x_bytes = std::max<int64_t>(P.x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
+        P.part_bytes = std::max<int64_t>(P.part_bytes, (int64_t)M.hmax * part_row);
+    }
+    P.part_bytes = 2 * round_up(P.part_bytes, 128);  // two row groups in flight
+    P.slot_bytes = round_up(P.slot_bytes, 128);
+    P.x_bytes = round_up(P.x_bytes, 128);
+    P.grid = cta;
+    return KQ_OK;
+}
+
+}  // namespace
+
+kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out) {
+    Plan &P = *out;
+    P = Plan{};
+    P.n = n;
+    P.ntok = ntok;
+    int ncta[KQ_MAX_SET];
+    split_ctas(mats, n, sms, ncta);
+    // The first level whose input records fit in shared memory beside at
+    // least three slots (two at the smallest level, or when a CTA has only
+    // two stages) is taken; if none fits, level 0 with the records in
+    // global memory.  The 1 KiB alignment of the dynamic region pads the
+    // static part to 1 KiB.
+    const int64_t budget = (int64_t)smem_optin - 1024;
+    for (int L = 0; L < kLevels && P.level < 0; ++L) {
+        if (plan_level(mats, n, ntok, ncta, L, P) != KQ_OK) continue;
+        const int64_t slots = (budget - 1024 - P.x_bytes - P.part_bytes) / P.slot_bytes;
+        const int64_t want = std::min<int64_t>(L == kLevels - 1 ? 2 : 3, std::max<int64_t>(2, P.stages));
+        if (slots >= want) P.level = L;
+    }
+    if (P.level >= 0) {
+        P.xsmem = true;
+    } else {
+        const kq_status ps = plan_level(mats, n, ntok, ncta, 0, P);
+        if (ps != KQ_OK) return ps;
+        P.x_bytes = 0;
+    }
+    const int64_t fixed = 1024 + P.x_bytes + P.part_bytes;
+    P.nslot = std::min<int64_t>(kq::kMaxSlots, (budget - fixed) / P.slot_bytes);
+    if (P.nslot < 2) return KQ_ERR_SHAPE;
+    P.smem = fixed + P.nslot * P.slot_bytes;
+    return KQ_OK;
+}
+
+}  // namespace kqplan
+
+extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
+                                int64_t *out, int cap) {
+    if (!mats || !out || n < 1 || n > KQ_MAX_SET || ntok < 1 || ntok > 8 || sms < 1) return -1;
+    if (cap < KQ_PLAN_HEAD + n * KQ_PLAN_MEMBER) return -1;
+    kqplan::Plan P;
+    const kq_status st = kqplan::plan_stream(mats, n, ntok, sms, smem_optin, &P);
+    int64_t *o = out;
+    *o++ = st;
+    *o++ = P.grid;
+    *o++ = P.level;
+    *o++ = P.xsmem ? 1 : 0;
+    *o++ = P.x_bytes;
+    *o++ = P.part_bytes;
+    *o++ = P.slot_bytes;
+    *o++ = P.nslot;
+    *o++ = P.smem;
+    *o++ = P.stages;
+    for (int i = 0; i < n; ++i) {
+        const kqplan::Member &M = P.m[i];
+        const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],
+                                           M.gq[0], M.gr[0], M.ng[1], M.gq[1], M.gr[1],
+                                           M.rmax, M.kb, M.seg, M.hmax, M.nh, M.hs[0],
+                                           M.hs[1], M.hs[2], M.hs[3], M.row_bytes};
+        for (int k = 0; k < KQ_PLAN_MEMBER; ++k) *o++ = v[k];
+    }
+    return 0;
+}

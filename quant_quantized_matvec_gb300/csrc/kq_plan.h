@@ -1,0 +1,50 @@
+// kq_plan.h -- launch geometry of the streaming kernel (host only).
+//
+// For a validated set: how many CTAs each member gets, how its rows split
+// into row groups, the stage shape [h rows][kb blocks], the ring of
+// shared-memory slots, and whether the input records fit in shared memory.
+// Pure arithmetic on the shapes and two device facts (SM count, opt-in
+// shared memory per CTA); kq_api.cu turns a plan into kernel parameters
+// and tensor maps, and kq_plan_describe (kq_internal.h) exposes it to the
+// host tests.
+#pragma once
+
+#include <stdint.h>
+
+#include "kq.h"
+
+namespace kqplan {
+
+constexpr int kMaxHeights = 4;  // distinct row-group heights per member
+
+struct Member {
+    int ncta = 0, cta_begin = 0;
+    int rows_q = 0, rows_r = 0;       // rows / ncta, rows % ncta
+    int ng[2] = {}, gq[2] = {}, gr[2] = {};  // groups of CTAs with rows_q (+1) rows
+    int rmax = 0;                     // rows per group at most
+    int kb = 0;                       // blocks per stage row
+    int seg = 0;                      // Q6_K: bytes between row segments in a slot
+    int nh = 0, hs[kMaxHeights] = {}; // group heights that occur
+    int hmax = 0;
+    int64_t row_bytes = 0;
+};
+
+struct Plan {
+    int n = 0, ntok = 0, grid = 0;
+    int level = -1;        // geometry level taken (records in global: level 0 geometry)
+    bool xsmem = false;    // input records in shared memory
+    int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0, nslot = 0, stages = 0;
+    int64_t smem = 0;      // dynamic shared memory of the launch
+    Member m[KQ_MAX_SET];
+};
+
+// Consumer cost per weight byte of Q6_K relative to Q4_K, in sixteenths
+// (measured: the Q6_K block loop spends more instructions per byte).
+constexpr int64_t kCostQ6 = 32;
+
+// The plan of one launch of `mats` (validated, 1..KQ_MAX_SET members,
+// ntok 1..8).  KQ_ERR_SHAPE when no geometry fits (the caller then uses
+// the direct-load kernel).
+kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out);
+
+}  // namespace kqplan

@@ -21,8 +21,8 @@ def lib():
     return _binding.load()
 
 
-def header_functions():
-    src = open(os.path.join(ROOT, "include", "kq.h")).read()
+def header_functions(name="kq.h"):
+    src = open(os.path.join(ROOT, "include", name)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kq_[a-z_]+)\s*\(", src)))
 
@@ -30,8 +30,11 @@ def header_functions():
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
     assert set(names) == set(_binding.SYMBOLS)
-    for n in names:
-        assert hasattr(lib, n), n
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            for n in header_functions(h):
+                assert hasattr(lib, n), f"{h}: {n}"
+    assert header_functions("kq_internal.h") == ["kq_plan_describe"]
 
 
 def test_block_and_matrix_bytes(lib):

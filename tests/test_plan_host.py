@@ -1,0 +1,142 @@
+"""The streaming kernel's launch plan (kq_plan.cu), checked on the host with
+no GPU through kq_plan_describe (include/kq_internal.h): for many shapes,
+formats, set compositions and ntok, the plan must fit the device, cover
+every row exactly once, keep stage task counts in the kernel's range and
+size Q6_K row segments for their misalignment."""
+import ctypes
+import itertools
+
+import numpy as np
+import pytest
+
+from quant_quantized_matvec_gb300 import _binding
+
+HEAD, MEMBER = 10, 20
+SMS, SMEM = 152, 232448          # GB300: SMs, opt-in shared memory per CTA
+BB = {12: 144, 13: 176, 14: 210}
+REC = {12: 832, 13: 832, 14: 1056}
+OK, SHAPE = 0, 2
+
+
+def plan(members, ntok, sms=SMS, smem=SMEM):
+    lib = _binding.load()
+    arr = (_binding.KqMat * len(members))()
+    for i, (fmt, rows, cols) in enumerate(members):
+        arr[i].fmt, arr[i].rows, arr[i].cols = fmt, rows, cols
+        arr[i].W = arr[i].x = arr[i].y = 16 << 20  # never read
+    out = (ctypes.c_int64 * (HEAD + MEMBER * len(members)))()
+    assert lib.kq_plan_describe(arr, len(members), ntok, sms, smem, out, len(out)) == 0
+    o = list(out)
+    head = dict(zip(["status", "grid", "level", "xsmem", "x_bytes", "part_bytes",
+                     "slot_bytes", "nslot", "smem", "stages"], o[:HEAD]))
+    keys = ["ncta", "cta_begin", "rows_q", "rows_r", "ng0", "gq0", "gr0", "ng1", "gq1",
+            "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes"]
+    mem = [dict(zip(keys, o[HEAD + MEMBER * i: HEAD + MEMBER * (i + 1)]))
+           for i in range(len(members))]
+    return head, mem
+
+
+def check(members, ntok, sms=SMS, smem=SMEM):
+    h, mem = plan(members, ntok, sms, smem)
+    if h["status"] != OK:
+        assert h["status"] == SHAPE
+        return h, mem
+    # the grid: every member gets CTAs, at most one per row, in order; one
+    # wave of one CTA per SM unless there are more members than SMs (CTAs
+    # never wait on one another, so a second wave is only slower)
+    assert 1 <= h["grid"] <= max(sms, len(members))
+    begin = 0
+    for (fmt, rows, cols), m in zip(members, mem):
+        assert m["cta_begin"] == begin and 1 <= m["ncta"] <= rows
+        begin += m["ncta"]
+        # every row once: ncta CTAs of rows_q or rows_q + 1 rows
+        assert m["rows_q"] * m["ncta"] + m["rows_r"] == rows and 0 <= m["rows_r"] < m["ncta"]
+        nb = cols // 256
+        assert m["row_bytes"] == nb * BB[fmt]
+        for big in (0, 1):
+            nn = m["rows_q"] + big
+            ng, gq, gr = m[f"ng{big}"], m[f"gq{big}"], m[f"gr{big}"]
+            # CTAs of rows_q + big rows exist only if rows_r > 0 (big) or
+            # rows_r < ncta (not big)
+            if nn == 0 or (big and m["rows_r"] == 0) or (not big and m["rows_r"] == m["ncta"]):
+                continue
+            assert ng * gq + gr == nn and 0 <= gr < ng
+            assert gq + (1 if gr else 0) <= m["rmax"] <= 32
+            assert gq + (1 if gr else 0) <= m["hmax"]
+        heights = [m[f"hs{j}"] for j in range(m["nh"])]
+        assert 1 <= m["nh"] <= 4 and max(heights) == m["hmax"]
+        # partials of a group fit 64 KiB
+        assert m["hmax"] * nb * ntok * 4 <= 64 * 1024
+        # stage rows: at most 2048 bytes, tasks below 2^12
+        assert 1 <= m["kb"] <= nb and m["kb"] * BB[fmt] <= 2048
+        assert ((m["hmax"] + 1) // 2) * m["kb"] < 4096
+        if fmt == 14:
+            # a segment holds kb blocks plus up to 14 bytes of misalignment
+            # at each end, and is an odd number of 16-byte units
+            assert m["seg"] >= m["kb"] * 210 + 28 and m["seg"] % 16 == 0 and (m["seg"] // 16) % 2 == 1
+            assert h["slot_bytes"] >= m["hmax"] * m["seg"]
+        else:
+            assert m["seg"] == 0 and h["slot_bytes"] >= m["hmax"] * m["kb"] * BB[fmt]
+            assert (m["kb"] * BB[fmt]) % 8 == 0  # tensor-map box rows in u64
+        assert h["part_bytes"] >= 2 * m["hmax"] * nb * ntok * 4
+        if h["xsmem"]:
+            assert h["x_bytes"] >= ntok * nb * REC[fmt]
+    assert begin == h["grid"]
+    # shared memory: records, partials and at least two slots within the opt-in
+    assert h["nslot"] >= 2 and h["nslot"] <= 32
+    assert h["smem"] == 1024 + h["x_bytes"] + h["part_bytes"] + h["nslot"] * h["slot_bytes"]
+    assert h["smem"] <= smem - 1024
+    if not h["xsmem"]:
+        assert h["x_bytes"] == 0 and h["level"] == -1
+    return h, mem
+
+
+def test_qkv_gate_set_plan_matches_its_profile():
+    """The QKV+gate set: 152 CTAs, records in shared memory, and the
+    dynamic shared memory the committed ncu capture shows (214,912 B)."""
+    qkv = [(12, 4096, 6656), (14, 256, 6656), (14, 256, 6656), (12, 4096, 6656)]
+    h, mem = check(qkv, 1)
+    assert h["status"] == OK and h["grid"] == 152 and h["xsmem"] == 1 and h["level"] == 0
+    assert h["smem"] == 214912
+    # Q6_K members get more CTAs per byte than Q4_K (cost weighting)
+    q4_share = mem[0]["ncta"] / (4096 * 26 * 144)
+    q6_share = mem[1]["ncta"] / (256 * 26 * 210)
+    assert q6_share > q4_share
+
+
+@pytest.mark.parametrize("fmt", [12, 13, 14])
+@pytest.mark.parametrize("ntok", [1, 2, 3, 5, 8])
+def test_single_matrices(fmt, ntok):
+    for rows, cols in itertools.product([1, 2, 31, 152, 153, 1000, 4096, 65536, 202048],
+                                        [256, 768, 2560, 6656, 19968, 33280]):
+        check([(fmt, rows, cols)], ntok)
+
+
+def test_random_sets():
+    rng = np.random.default_rng(5)
+    planned = 0
+    for _ in range(400):
+        n = int(rng.integers(1, 17))
+        ntok = int(rng.integers(1, 9))
+        members = [(int(rng.choice([12, 13, 14])), int(rng.integers(1, 5000)),
+                    256 * int(rng.choice([1, 3, 10, 26, 78]))) for _ in range(n)]
+        h, _ = check(members, ntok)
+        planned += h["status"] == OK
+    assert planned > 300
+
+
+def test_more_members_than_sms_and_small_devices():
+    check([(12, 64, 512)] * 16, 1, sms=8)
+    check([(14, 3, 6656), (12, 5000, 6656)], 4, sms=16, smem=101376)
+
+
+def test_shapes_the_stream_kernel_cannot_stage():
+    """Partials of one row beyond 64 KiB (cols 2^20 at ntok 8) leave no
+    geometry: the direct kernel runs instead."""
+    h, _ = plan([(12, 64, 1 << 20)], 8)
+    assert h["status"] == SHAPE
+
+
+def test_plan_is_deterministic():
+    members = [(12, 4096, 6656), (14, 256, 6656), (13, 777, 2560)]
+    assert plan(members, 3) == plan(members, 3)
