@@ -23,17 +23,20 @@
  * Conventions for every entry point below
  *   - W is a DEVICE pointer (cudaMalloc / torch CUDA storage on the current
  *     device).  x and y are device pointers too, or pointers into pinned
- *     host memory (cudaHostAlloc, cudaHostRegister, torch pin_memory),
- *     which the kernels read and write in place over the host link -- on
- *     GB300 (Grace) that saves the separate copy of the outputs back to
- *     the host.  Managed memory is accepted for x and y.  Anything else
- *     (pageable host memory, another device's memory) is KQ_ERR_MEMORY.
- *     All memory is owned by the caller.  The library
+ *     host memory (cudaHostAlloc, cudaHostRegister, torch pin_memory).  A
+ *     host y is written in place by the kernel over the host link.  Host
+ *     x planes are copied once into a stream-ordered device temporary by a
+ *     small staging kernel, which the matvec overlaps with its weight
+ *     stream (kq_matvec_noalloc instead reads them in place).  On GB300
+ *     (Grace) this replaces the separate copies in and out.  Managed memory
+ *     is accepted for x and y.  Anything else (pageable host memory,
+ *     another device's memory) is KQ_ERR_MEMORY.  All memory is owned by
+ *     the caller.  The library
  *     keeps no pointer after a call returns and never synchronizes.  Its
- *     one allocation is a stream-ordered temporary (cudaMallocAsync /
- *     cudaFreeAsync on `stream`) for the input records of calls whose
- *     records do not fit in shared memory; kq_matvec_noalloc allocates
- *     nothing.
+ *     allocations are stream-ordered temporaries (cudaMallocAsync /
+ *     cudaFreeAsync on `stream`): the input records of calls whose records
+ *     do not fit in shared memory, and staged host inputs;
+ *     kq_matvec_noalloc allocates nothing.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream) and may be captured in a CUDA graph.
  *   - Every argument is validated on the host before anything is launched;

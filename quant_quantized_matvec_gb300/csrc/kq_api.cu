@@ -82,6 +82,29 @@ __global__ void __launch_bounds__(kPrepThreads) kq_xprep(const __grid_constant__
     build_record_half(v, p.rec[mi] + (int64_t)(i >> 1) * rec_bytes(q6), i & 1, q6, lane);
 }
 
+// Input planes that live in host memory, copied once into device memory:
+// one float4 per thread.  It lets the next kernel on the stream launch at
+// once, so that kernel streams its weights while this copy runs.
+struct StageParams {
+    const float4 *src[KQ_MAX_SET];
+    float4 *dst[KQ_MAX_SET];
+    int64_t first[KQ_MAX_SET + 1];  // first float4 of each plane; first[n] = total
+    int n;
+};
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads) kq_xstage(const __grid_constant__ StageParams p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t i = (int64_t)blockIdx.x * kStageThreads + threadIdx.x;
+    if (i >= p.first[p.n]) return;
+    int k = 0;
+#pragma unroll 1
+    for (int j = 1; j < p.n; ++j)
+        if (i >= p.first[j]) k = j;
+    const int64_t o = i - p.first[k];
+    p.dst[k][o] = p.src[k][o];
+}
+
 }  // namespace kq
 
 namespace {
@@ -159,7 +182,9 @@ kq_status validate_set(const kq_mat *mats, int n, int ntok) {
 // space (pinned: cudaHostAlloc / cudaHostRegister), which the kernels read
 // and write in place over the host link.  `alias` is the address the device
 // uses.  A failed query is KQ_ERR_CUDA; anything else is KQ_ERR_MEMORY.
-kq_status device_address(const void *p, int dev, bool host_ok, const void **alias) {
+kq_status device_address(const void *p, int dev, bool host_ok, const void **alias,
+                         bool *in_host) {
+    *in_host = false;
     cudaPointerAttributes a{};
     const cudaError_t e = cudaPointerGetAttributes(&a, p);
     if (e != cudaSuccess) {
@@ -177,6 +202,7 @@ kq_status device_address(const void *p, int dev, bool host_ok, const void **alia
     case cudaMemoryTypeHost:
         if (!host_ok || !a.devicePointer) return KQ_ERR_MEMORY;
         *alias = a.devicePointer;
+        *in_host = true;
         return KQ_OK;
     default:
         return KQ_ERR_MEMORY;
@@ -184,22 +210,26 @@ kq_status device_address(const void *p, int dev, bool host_ok, const void **alia
 }
 
 // The set with every pointer checked and replaced by its device address;
-// a pointer that repeats (a shared x) is looked up once.
-kq_status resolve_set(const kq_mat *mats, int n, int dev, kq_mat *out) {
+// a pointer that repeats (a shared x) is looked up once.  x_host[i]: member
+// i's x is in host memory.
+kq_status resolve_set(const kq_mat *mats, int n, int dev, kq_mat *out, bool *x_host) {
     for (int i = 0; i < n; ++i) {
         out[i] = mats[i];
+        x_host[i] = false;
         for (int k = 0; k < 3; ++k) {
             const void *p = k == 0 ? mats[i].W : k == 1 ? (const void *)mats[i].x : (const void *)mats[i].y;
             const void *q = nullptr;
+            bool host = false;
             for (int j = 0; j < i && !q; ++j) {
                 if (mats[j].W == p) q = out[j].W;
-                else if ((const void *)mats[j].x == p) q = out[j].x;
+                else if ((const void *)mats[j].x == p) q = out[j].x, host = x_host[j];
                 else if ((const void *)mats[j].y == p) q = out[j].y;
             }
             if (!q) {
-                const kq_status st = device_address(p, dev, k != 0, &q);
+                const kq_status st = device_address(p, dev, k != 0, &q, &host);
                 if (st != KQ_OK) return st;
             }
+            if (k == 1) x_host[i] = host;
             if (k == 0) out[i].W = q;
             else if (k == 1) out[i].x = static_cast<const float *>(q);
             else out[i].y = static_cast<float *>(const_cast<void *>(q));
@@ -409,7 +439,7 @@ std::atomic<int> g_overlap{0};
 // Plan the streaming kernel.  Returns KQ_OK after launching, or
 // KQ_ERR_SHAPE when the shapes cannot be staged (caller falls back).
 kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
-                     const DeviceInfo &info, bool *launched) {
+                     const DeviceInfo &info, bool after_stage, bool *launched) {
     *launched = false;
     static kq::StreamParams p;  // ~10 KB: kept off the stack
     static std::mutex pmu;
@@ -461,7 +491,10 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.slot_bytes = (int)P.slot_bytes;
     p.x_bytes = (int)P.x_bytes;
     p.part_bytes = (int)P.part_bytes;
-    p.overlap = g_overlap.load() ? 1 : 0;
+    // Launch overlap: as set by kq_set_overlap, and always right after the
+    // staging kernel, which writes nothing this launch reads before its
+    // griddepcontrol.wait.
+    p.overlap = (g_overlap.load() || after_stage) ? 1 : 0;
     for (int hp = 1; hp <= kq::kMaxHinv; ++hp) p.hinv[hp] = ((1u << 20) + hp - 1) / hp;
     p.hinv[0] = 1u << 20;
     p.err = info.err;
@@ -541,7 +574,50 @@ void token_chunk(const kq_mat *mats, int n, int t0, kq_mat *out) {
     }
 }
 
-kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream);
+kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream, bool after_stage);
+
+// Inputs in host memory: every distinct such x plane (all ntok columns) is
+// copied once into one stream-ordered device temporary by kq_xstage, and
+// the members read it there instead of across the host link from every CTA.
+// *buf is the temporary (nullptr: nothing to stage).
+cudaError_t stage_inputs(kq_mat *mats, int n, int ntok, const bool *x_host, cudaStream_t s,
+                         void **buf) {
+    *buf = nullptr;
+    kq::StageParams p{};
+    const float *planes[KQ_MAX_SET];
+    int64_t off[KQ_MAX_SET], total = 0;
+    int of[KQ_MAX_SET];  // plane of each member (-1: not staged)
+    for (int i = 0; i < n; ++i) {
+        of[i] = -1;
+        if (!x_host[i]) continue;
+        for (int k = 0; k < p.n && of[i] < 0; ++k)
+            if (planes[k] == mats[i].x) of[i] = k;
+        if (of[i] >= 0) continue;
+        of[i] = p.n;
+        planes[p.n] = mats[i].x;
+        const int64_t n4 = (int64_t)ntok * mats[i].cols / 4;
+        p.src[p.n] = reinterpret_cast<const float4 *>(mats[i].x);
+        off[p.n] = total;
+        total += (n4 * 16 + 255) / 256 * 256;
+        p.first[p.n + 1] = p.first[p.n] + n4;
+        ++p.n;
+    }
+    if (p.n == 0) return cudaSuccess;
+    cudaError_t e = cudaMallocAsync(buf, (size_t)total, s);
+    if (e != cudaSuccess) {
+        *buf = nullptr;
+        return e;
+    }
+    for (int k = 0; k < p.n; ++k)
+        p.dst[k] = reinterpret_cast<float4 *>(static_cast<uint8_t *>(*buf) + off[k]);
+    const int64_t blocks = (p.first[p.n] + kq::kStageThreads - 1) / kq::kStageThreads;
+    kq::kq_xstage<<<(unsigned)blocks, kq::kStageThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i)
+        if (of[i] >= 0) mats[i].x = reinterpret_cast<const float *>(p.dst[of[i]]);
+    return cudaSuccess;
+}
 
 kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
     const kq_status v = validate_set(in, n, ntok);
@@ -553,30 +629,49 @@ kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
         return KQ_ERR_CUDA;
     }
     kq_mat mats[KQ_MAX_SET];
-    const kq_status r = resolve_set(in, n, dev, mats);
+    bool x_host[KQ_MAX_SET];
+    const kq_status r = resolve_set(in, n, dev, mats, x_host);
     if (r != KQ_OK) return r;
+    cudaStream_t s = (cudaStream_t)stream;
+    void *staged = nullptr;
+    cudaError_t se = stage_inputs(mats, n, ntok, x_host, s, &staged);
+    if (se != cudaSuccess) {
+        if (staged) cudaFreeAsync(staged, s);
+        g_last_cuda_error = (int)se;
+        return KQ_ERR_CUDA;
+    }
+    const bool after = staged != nullptr;
     const int cn = launch_ntok();
-    if (ntok <= cn) return run_chunk(mats, n, ntok, stream);
     // near-equal chunks: the first `rem` take one column more
     const int nch = (ntok + cn - 1) / cn, base = ntok / nch, rem = ntok % nch;
     kq_mat part[KQ_MAX_SET];
-    int kernels = 0, launches = 0;
-    for (int ci = 0, t0 = 0; ci < nch; ++ci) {
+    int kernels = 0, launches = after ? 1 : 0;
+    kq_status st = KQ_OK;
+    for (int ci = 0, t0 = 0; ci < nch && st == KQ_OK; ++ci) {
         const int nt = base + (ci < rem ? 1 : 0);
         token_chunk(mats, n, t0, part);
         t0 += nt;
-        const kq_status st = run_chunk(part, n, nt, stream);
-        if (st != KQ_OK) return st;
+        st = run_chunk(part, n, nt, stream, after);
         kernels |= g_last_kernels;
         launches += g_last_launches;
     }
+    if (staged) {
+        se = cudaFreeAsync(staged, s);
+        if (st == KQ_OK && se != cudaSuccess) {
+            g_last_cuda_error = (int)se;
+            st = KQ_ERR_CUDA;
+        }
+    }
+    if (st != KQ_OK) return st;
     g_last_kernels = kernels;
     g_last_launches = launches;
     return KQ_OK;
 }
 
 // One launch's worth (ntok <= kLaunchNtok) of a validated set.
-kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream) {
+// after_stage: the inputs were just staged by kq_xstage (kernels that can
+// overlap it are launched to do so).
+kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream, bool after_stage) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     DeviceInfo info;
@@ -589,7 +684,7 @@ kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream) {
     const int choice = kernel_choice();
     if (choice != 1) {
         bool launched = false;
-        const kq_status st = run_stream(mats, n, ntok, s, info, &launched);
+        const kq_status st = run_stream(mats, n, ntok, s, info, after_stage, &launched);
         if (launched || choice == 2) return st;
     }
     return run_direct(mats, n, ntok, s, info);
@@ -632,8 +727,10 @@ kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
     }
+    // host-memory inputs are read in place here: staging them would allocate
     kq_mat m;
-    const kq_status r = resolve_set(&in, 1, dev, &m);
+    bool x_host = false;
+    const kq_status r = resolve_set(&in, 1, dev, &m, &x_host);
     if (r != KQ_OK) return r;
     int launches = 0;
     for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {

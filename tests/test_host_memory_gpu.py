@@ -89,6 +89,54 @@ def test_noalloc_with_host_output():
     assert np.array_equal(bits(yh.numpy()), bits(yd.host()))
 
 
+def test_noalloc_reads_host_inputs_in_place():
+    """kq_matvec_noalloc does not stage host inputs (that would allocate): its
+    kernels read x across the host link; the results are the same."""
+    lib = _binding.load()
+    fmt, rows, cols, ntok = kq.Q6_K, 150, 2560, 3
+    W, x = C.case(fmt, rows, cols, ntok, "host/noalloc/x")
+    Wd = C.to_dev(W)
+    xh = torch.from_numpy(x).pin_memory()
+    ya, yb = C.Guarded(ntok, rows), C.Guarded(ntok, rows)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for fn, xp, g in ((lib.kq_matvec_noalloc, xh.data_ptr(), ya),
+                      (lib.kq_matvec, C.to_dev(x).data_ptr(), yb)):
+        assert fn(fmt, ctypes.c_void_p(Wd.data_ptr()), rows, cols, ctypes.c_void_p(xp),
+                  ctypes.c_void_p(g.y.data_ptr()), ntok, s) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(ya.host()), bits(yb.host()))
+
+
+def test_staged_inputs_shared_and_separate_in_a_set():
+    """Host inputs of a set, one shared by two members and one of its own,
+    each staged once; with overlap on and off."""
+    ntok, cols = 3, 1536
+    xa = C.case(kq.Q4_K, 1, cols, ntok, "host/stage/xa")[1]
+    xb = C.case(kq.Q4_K, 1, cols, ntok, "host/stage/xb")[1]
+    xah, xbh = torch.from_numpy(xa).pin_memory(), torch.from_numpy(xb).pin_memory()
+    specs = [(kq.Q4_K, 300, xah, xa), (kq.Q6_K, 77, xah, xa), (kq.Q5_K, 129, xbh, xb)]
+    prev = kq.set_overlap(False)
+    try:
+        for overlap in (False, True):
+            kq.set_overlap(overlap)
+            members, refs = [], []
+            for i, (fmt, rows, xh, x) in enumerate(specs):
+                Wd = C.to_dev(C.case(fmt, rows, cols, 1, f"host/stage/W{i}")[0])
+                g = C.Guarded(ntok, rows)
+                members.append((fmt, Wd, rows, cols, xh, g.y))
+                ref = C.Guarded(ntok, rows)
+                kq.matvec(fmt, Wd, rows, cols, C.to_dev(x), y=ref.y)
+                refs.append((g, ref))
+            kq.matvec_set(members)
+            assert kq.last_launch_count() == 2  # the staging kernel and the set
+            torch.cuda.synchronize()
+            for g, ref in refs:
+                assert np.array_equal(bits(g.host()), bits(ref.host()))
+    finally:
+        kq.set_overlap(prev)
+    assert not kq.device_error()
+
+
 def test_refuses_memory_the_device_cannot_address():
     """Pageable host memory for y or x, and W outside device memory, return
     KQ_ERR_MEMORY with nothing launched (the output is left untouched)."""
