@@ -243,7 +243,10 @@ __device__ __forceinline__ void block_q45(const BS (&B)[R], const XR &xr,
         for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.0f;
     }
     constexpr int QS = Q5 ? 3 : 1;
-#pragma unroll 1
+    // one token: the four groups fully unrolled, for independent work to
+    // interleave (measured 3% faster); more tokens keep the loop, whose
+    // unrolled form spills
+#pragma unroll(NTOK == 1 ? 4 : 1)
     for (int g = 0; g < 4; ++g) {
         uint32_t lo[R][8], hi[R][8];
 #pragma unroll
