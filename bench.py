@@ -156,6 +156,23 @@ def recorded_traffic(workload_name, ntok):
     return None
 
 
+def max_over_ranks(value, dist, device=None):
+    """The largest of every rank's value (a job takes as long as its slowest
+    rank); `value` itself when the run is not distributed."""
+    if not dist:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes, steps, world, ms):
+    """Whole-job throughput: the bytes every rank processed over the job's
+    time (the slowest rank's), in GB/s."""
+    return step_bytes * steps * world / (ms * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -333,11 +350,7 @@ def run_ours(args, rank, world, dist):
         wall = time.perf_counter() - t_wall
         if dist:
             dist.barrier()
-        ms = ev0.elapsed_time(ev1)
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
         return ms, wall, (reps, rem)
 
     overlap = not args.no_overlap
@@ -351,8 +364,7 @@ def run_ours(args, rank, world, dist):
     clocks = sampler.stop()
     kernels = kq.last_kernels()
     launches_per_step = kq.last_launch_count()
-    total_bytes = step_bytes * K * world
-    gbs = total_bytes / (ms * 1e-3) / 1e9
+    gbs = job_gbs(step_bytes, K, world, ms)
     us_per_step = ms * 1e3 / K
 
     # End to end through the public API, every step: the call takes x and y
@@ -401,19 +413,14 @@ def run_ours(args, rank, world, dist):
                 one(i)
         e1.record(stream)
         torch.cuda.synchronize()
-        t_ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([t_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_ms = float(t.item())
-        return t_ms
+        return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     ems = e2e(True)
     y_direct = y_host.clone()
     ems_copy = e2e(False)
     # the last step wrote the same outputs both ways
     e2e_same = bool(torch.equal(y_direct.view(torch.int32), y_host.view(torch.int32)))
-    e2e_gbs = step_bytes * Ke * world / (ems * 1e-3) / 1e9
+    e2e_gbs = job_gbs(step_bytes, Ke, world, ems)
 
     peak, peak_kind = peaks()
     traffic = recorded_traffic(args.workload, ntok)
@@ -451,11 +458,11 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": K * launches_per_step,
         "launch_overlap": overlap,
         "warm_l2": ({"us_per_call": round(ms_warm * 1e3 / Kw, 3),
-                     "value": round(step_bytes * Kw * world / (ms_warm * 1e-3) / 1e9, 2),
+                     "value": round(job_gbs(step_bytes, Kw, world, ms_warm), 2),
                      "note": "warm, L2-resident: one weight copy reused every call "
                              "(not an HBM number)"} if ms_warm else None),
         "serial": {"us_per_call": round(ms_serial * 1e3 / K, 3),
-                   "value": round(step_bytes * K * world / (ms_serial * 1e-3) / 1e9, 2),
+                   "value": round(job_gbs(step_bytes, K, world, ms_serial), 2),
                    "note": "same steps with launch overlap off (each call "
                            "starts after the previous one completes)"},
         "roofline": {
@@ -479,7 +486,7 @@ def run_ours(args, rank, world, dist):
                         "the matvec overlaps with its weight stream, and the matvec "
                         "writes y straight into host memory over the host link",
                 "outputs_equal_copy_path": e2e_same,
-                "copy_path": {"value": round(step_bytes * Ke * world / (ems_copy * 1e-3) / 1e9, 2),
+                "copy_path": {"value": round(job_gbs(step_bytes, Ke, world, ems_copy), 2),
                               "us_per_step": round(ems_copy * 1e3 / Ke, 3),
                               "path": "x and y in device memory, with async copies "
                                       "from and to pinned host memory around each call"}},
@@ -558,12 +565,8 @@ def run_embed(args, rank, world, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    gbs = step_bytes * K * world / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    gbs = job_gbs(step_bytes, K, world, ms)
     # end to end: ids from pinned host memory, rows back to pinned host memory
     ids_host = torch.from_numpy(
         rng.integers(0, rows, size=n).astype(np.int32)).pin_memory()
