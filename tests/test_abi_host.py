@@ -22,7 +22,8 @@ def lib():
 
 
 def header_functions(name="kq.h"):
-    src = open(os.path.join(ROOT, "include", name)).read()
+    with open(os.path.join(ROOT, "include", name)) as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kq_[a-z_]+)\s*\(", src)))
 
