@@ -358,7 +358,8 @@ def run_ours(args, rank, world, dist):
 
     def timed(overlap, sampler=None, stepfn=step, K=K):
         """K steps replayed from CUDA graphs of L steps, captured with the
-        given launch-overlap setting; -> ms (max over ranks), wall s."""
+        given launch-overlap setting; -> ms (max over ranks), wall s,
+        (replays, remainder steps), µs per call of each main-graph replay."""
         kq.set_overlap(overlap)
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
@@ -384,14 +385,18 @@ def run_ours(args, rank, world, dist):
             time.sleep(0.3)
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
+        # one event after each replay of the main graph: per-replay times
+        # for the median (recorded between replays, on the same stream)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
         ev0.record(stream)
         with torch.cuda.stream(stream):
-            for _ in range(reps):
+            for r in range(reps):
                 g_main.replay()
+                evs[r].record(stream)
             if g_rem is not None:
                 g_rem.replay()
         ev1.record(stream)
@@ -400,16 +405,19 @@ def run_ours(args, rank, world, dist):
         if dist:
             dist.barrier()
         ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
-        return ms, wall, (reps, rem)
+        per_replay = [ev0.elapsed_time(evs[0])] + [
+            evs[r - 1].elapsed_time(evs[r]) for r in range(1, reps)]
+        return ms, wall, (reps, rem), [1e3 * t / L for t in per_replay]
 
     overlap = not args.no_overlap
-    ms_serial, _, _ = timed(False)
+    ms_serial = timed(False)[0]
     # warm: the same calls on one weight copy, which stays in L2 when it fits
     Kw = min(K, 20000)
     ms_warm = (timed(overlap, stepfn=lambda i: step(0), K=Kw)[0]
                if copies > 1 else None)
     sampler = ClockSampler(dev.index)
-    ms, wall, (reps, rem) = timed(overlap, sampler)
+    ms, wall, (reps, rem), per_replay = timed(overlap, sampler)
+    per_replay = sorted(per_replay)
     clocks = sampler.stop()
     kernels = kq.last_kernels()
     launches_per_step = kq.last_launch_count()
@@ -505,6 +513,11 @@ def run_ours(args, rank, world, dist):
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "gpu_launches": K * launches_per_step,
+        "replays": {"n": len(per_replay), "calls_each": L,
+                    "median_us_per_call": round(float(np.median(per_replay)), 3),
+                    "min_us_per_call": round(per_replay[0], 3),
+                    "max_us_per_call": round(per_replay[-1], 3),
+                    "note": "per replay of the main graph inside the timed region (this rank)"},
         "launch_overlap": overlap,
         "warm_l2": ({"us_per_call": round(ms_warm * 1e3 / Kw, 3),
                      "value": round(job_gbs(step_bytes, Kw, world, ms_warm), 2),

@@ -4,6 +4,8 @@ pins would catch a dropped term, a wrong sign, index, shift or field offset.
 """
 import os
 
+import numpy as np
+
 import pytest
 
 import oracle
@@ -65,5 +67,8 @@ def test_mutant_is_caught(name, tmp_path):
     path = tmp_path / "kq_oracle_mutant.c"
     path.write_text(src.replace(old, new))
     lib = oracle.compile_library(str(path), str(tmp_path / "libmut.so"))
-    failed = _run_all(oracle.Oracle(lib))
+    # a mutant may produce non-finite weights; numpy's notes about them are
+    # beside the point, the pins' verdict is what counts
+    with np.errstate(all="ignore"):
+        failed = _run_all(oracle.Oracle(lib))
     assert failed, f"mutant {name} passed every pin"
