@@ -20,10 +20,14 @@ steps on all ranks / max-over-ranks elapsed time.  By default the calls run
 with launch overlap on (kq_set_overlap: a call streams its weights while the
 previous call finishes and reads x only after that call completes); the
 same K steps with overlap off are timed too and reported as `serial`
-(--no-overlap makes them the headline).  `e2e` times the public
-Python API with the per-step input x copied from pinned host memory and the
-outputs copied back inside the timed region (weights stay resident, as model
-weights do).  `cpu_baseline` times the CPU oracle on a bounded sample.
+(--no-overlap makes them the headline).  `replays` gives the median,
+minimum and maximum us per call over the graph replays of the timed region.
+`e2e` times the public Python API with x and y in pinned host memory: each
+call copies its x in and writes its y back inside the timed region (weights
+stay resident, as model weights do); the same steps with explicit copies
+around device buffers are reported beside it.  `cpu_baseline` times the CPU
+oracle on a bounded sample, single-threaded and (`all_cores`) with the rows
+split over every host core.
 
 --impl reference times the CPU oracle itself (single thread) on a bounded
 sample of the same workload each step, and prints the same JSON line with
