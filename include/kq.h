@@ -48,6 +48,21 @@
  *   - Results are deterministic: a row's arithmetic depends only on the
  *     format, cols, ntok and that row's bytes and inputs -- not on the grid,
  *     the number of rows, or which other matrices share the launch.
+ *   - Accuracy and its precondition.  Products are summed exactly in
+ *     integers over inputs held in 24-bit fixed point, one power-of-two step
+ *     per group of 32 consecutive inputs set by the group's largest
+ *     magnitude (2^(E-1) <= max|x| < 2^E, E clamped to [-100, 128]).  The
+ *     input rounding adds at most  B_i = sum_g 2^(E_g - 24) * sum_{j in g}
+ *     |W_ij|  to output i's error; the sub-block sums add f32 roundings
+ *     far smaller.  The result is within |y - y_exact| <= 1e-4 * S_i +
+ *     1e-6, S_i = sum_j |W_ij x_j|, whenever B_i is below that bound:
+ *     PRECONDITION, in words: no input is more than about 10^4 times the
+ *     typical magnitude of its group of 32 while sitting on a (near) zero
+ *     weight.  Inputs drawn from one distribution (as activations are) are
+ *     hundreds of times inside it; an input of 1e6 on an exactly zero
+ *     weight among N(0,1) inputs is about 10x outside it, though still
+ *     within B.  NaN or infinite inputs make the outputs that read their
+ *     group NaN.
  */
 #ifndef KQ_H
 #define KQ_H
@@ -74,9 +89,10 @@ typedef enum kq_status {
     KQ_ERR_NULL = 4,    /* a required pointer is NULL                         */
     KQ_ERR_ALIGN = 5,   /* W or x not 16-byte aligned, or y not 4-byte aligned */
     KQ_ERR_ALIAS = 6,   /* an output overlaps an input or another output      */
-    KQ_ERR_COUNT = 7,   /* set size outside 1..KQ_MAX_SET                     */
-    KQ_ERR_CUDA = 8,    /* the CUDA launch failed (see kq_last_cuda_error)    */
-    KQ_ERR_TIMEOUT = 9, /* a bounded device-side wait expired                 */
+    KQ_ERR_CUDA = 7,    /* a CUDA call failed (see kq_last_cuda_error)        */
+    KQ_ERR_TIMEOUT = 8, /* a bounded device-side wait expired                 */
+    /* codes beyond the eight of the problem statement's boundary:          */
+    KQ_ERR_COUNT = 9,   /* set size outside 1..KQ_MAX_SET                     */
     KQ_ERR_LIMIT = 10,  /* kq_matvec_noalloc: inputs beyond its fixed buffer  */
     KQ_ERR_MEMORY = 11  /* W not in this device's memory, or x / y in memory
                            the device cannot address (pageable host memory,
@@ -172,15 +188,20 @@ kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream);
  *   out[i][j] = W[ids[i], j],  i < n, j < cols
  *
  *   fmt, W, rows, cols  as kq_matvec (W device, 16-byte aligned).
- *   ids   device int32[n]; an index outside [0, rows) yields a row of NaN.
+ *   ids   device or pinned host int32[n], 4-byte aligned; an index outside
+ *         [0, rows) yields a row of NaN.
  *   n     rows to gather, 0..2^31-1 (0: nothing is enqueued).
- *   out   device f32 [n][cols], 16-byte aligned, overwritten; must not
- *         overlap W or ids.
+ *   out   device or pinned host f32 [n][cols], 16-byte aligned,
+ *         overwritten; must not overlap W or ids.
  *
  * Each value is the correctly rounded weight: d*sc*q - dmin*m (Q4_K,
  * Q5_K) or d*sc*(q-32) (Q6_K) with only the final subtraction rounded
  * (the products are exact in f32), so any exact evaluation gives the same
- * bits.  Validation and status codes as kq_matvec.
+ * bits.  Validation and status codes as kq_matvec: after the host-only
+ * checks the three pointers are checked with cudaPointerGetAttributes, and
+ * W outside this device's memory, or ids / out in memory the device cannot
+ * address (pageable host memory, another device's memory), return
+ * KQ_ERR_MEMORY with nothing enqueued.  Allocates nothing.
  */
 kq_status kq_dequant_rows(int fmt, const void *W, int64_t rows, int64_t cols,
                           const int32_t *ids, int64_t n, float *out, void *stream);
@@ -230,7 +251,7 @@ int kq_set_overlap(int enable);
 
 /*
  * Kernels the calling thread's most recent successful kq_matvec /
- * kq_matvec_set call enqueued, as bits: 1 = the direct-load kernel, 2 = the
+ * kq_matvec_set / kq_matvec_noalloc call enqueued, as bits: 1 = the direct-load kernel, 2 = the
  * TMA-streaming kernel, 4 = the pass that writes input records to global
  * memory first (when they do not fit in shared memory).  0 before any call.
  */

@@ -1,6 +1,6 @@
 /*
- * kq_internal.h -- introspection of libkq.so for its host tests.  Not part
- * of the matvec path: no call here touches a GPU or launches anything.
+ * kq_internal.h -- introspection and test hooks of libkq.so.  Not part of
+ * the matvec path: no call here touches a GPU or launches anything.
  */
 #ifndef KQ_INTERNAL_H
 #define KQ_INTERNAL_H
@@ -36,6 +36,23 @@ extern "C" {
  */
 int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
                      int64_t *out, int cap);
+
+/*
+ * Test hook for failure reporting: the wall-time limit, in nanoseconds, of
+ * every wait the streaming kernel makes on a shared-memory barrier (and of
+ * its producer's wait for the input loads), for launches enqueued after
+ * this call; 0 restores the default of 2 s.  Returns the previous setting
+ * (0 = default).  Process-wide.
+ *
+ * A limit far below the time the weights take to arrive makes waits expire
+ * on purpose.  The kernel then does what it does on a real expiry: the CTA
+ * sets its abort flag and the device error word (kq_device_error reports
+ * KQ_ERR_TIMEOUT), stops issuing copies, waits -- always with the default
+ * limit -- for the copies it had issued, and writes NaN to the rows it had
+ * not finished.  Nothing hangs or faults, and the next launch made with the
+ * default limit computes normally.
+ */
+unsigned long long kq_set_wait_limit_ns(unsigned long long ns);
 
 #ifdef __cplusplus
 }

@@ -19,6 +19,8 @@ Q4_K, Q5_K, Q6_K = 12, 13, 14
 FORMATS = (Q4_K, Q5_K, Q6_K)
 MAX_NTOK = 16
 MAX_SET = 16
+# status codes of include/kq.h that the wrappers act on
+KQ_ERR_CUDA, KQ_ERR_TIMEOUT = 7, 8
 
 
 class KQError(RuntimeError):
@@ -26,7 +28,7 @@ class KQError(RuntimeError):
         lib = _binding.load()
         msg = lib.kq_status_str(status).decode()
         extra = ""
-        if status == 8:
+        if status == KQ_ERR_CUDA:
             extra = f" (cudaError {lib.kq_last_cuda_error()})"
         super().__init__(f"{where}: {_binding.STATUS.get(status, status)}: "
                          f"{msg}{extra}")
@@ -196,6 +198,6 @@ def device_error(clear: bool = True) -> bool:
     """True if a kernel on the current device reported an expired wait
     (synchronous read of the device error word)."""
     st = _lib().kq_device_error(1 if clear else 0)
-    if st == 8:
+    if st == KQ_ERR_CUDA:
         raise KQError(st, "kq_device_error")
-    return st == 9
+    return st == KQ_ERR_TIMEOUT

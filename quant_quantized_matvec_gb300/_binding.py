@@ -14,7 +14,7 @@ from . import build as _build
 STATUS = {
     0: "KQ_OK", 1: "KQ_ERR_FORMAT", 2: "KQ_ERR_SHAPE", 3: "KQ_ERR_NTOK",
     4: "KQ_ERR_NULL", 5: "KQ_ERR_ALIGN", 6: "KQ_ERR_ALIAS",
-    7: "KQ_ERR_COUNT", 8: "KQ_ERR_CUDA", 9: "KQ_ERR_TIMEOUT",
+    7: "KQ_ERR_CUDA", 8: "KQ_ERR_TIMEOUT", 9: "KQ_ERR_COUNT",
     10: "KQ_ERR_LIMIT", 11: "KQ_ERR_MEMORY",
 }
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
@@ -83,6 +83,8 @@ def load(path: str | None = None):
         lib.kq_set_overlap.restype = i32
         lib.kq_plan_describe.argtypes = [vp, i32, i32, i32, i32, vp, i32]
         lib.kq_plan_describe.restype = i32
+        lib.kq_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.kq_set_wait_limit_ns.restype = ctypes.c_ulonglong
         lib.kq_last_kernels.argtypes = []
         lib.kq_last_kernels.restype = i32
         lib.kq_last_launch_count.argtypes = []

@@ -13,6 +13,7 @@
 #include <unordered_map>
 
 #include "kq.h"
+#include "kq_internal.h"
 #include "kq_launch.cuh"
 #include "kq_plan.h"
 
@@ -435,6 +436,9 @@ bool tensor_map(const void *W, int64_t rows, int64_t row_bytes, int box_w, int b
 
 // Launch overlap with the preceding kernel (kq_set_overlap).
 std::atomic<int> g_overlap{0};
+// Wall-time limit of the streaming kernel's waits (kq_set_wait_limit_ns;
+// 0: the default).
+std::atomic<unsigned long long> g_wait_ns{0};
 
 // Plan the streaming kernel.  Returns KQ_OK after launching, or
 // KQ_ERR_SHAPE when the shapes cannot be staged (caller falls back).
@@ -498,6 +502,8 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     for (int hp = 1; hp <= kq::kMaxHinv; ++hp) p.hinv[hp] = ((1u << 20) + hp - 1) / hp;
     p.hinv[0] = 1u << 20;
     p.err = info.err;
+    const unsigned long long wl = g_wait_ns.load();
+    p.wait_ns = wl ? wl : kq::kWaitLimitNs;
     const size_t smem = (size_t)P.smem;
     *launched = true;
     GlobalRecords gr;
@@ -852,8 +858,24 @@ kq_status kq_dequant_rows(int fmt, const void *W, int64_t rows, int64_t cols,
     const Range rw{(uintptr_t)W, (uintptr_t)W + (uintptr_t)(rows * (cols / 256) * bb)};
     const Range ri{(uintptr_t)ids, (uintptr_t)ids + (uintptr_t)(n * (int64_t)sizeof(int32_t))};
     if (overlaps(ro, rw) || overlaps(ro, ri)) return KQ_ERR_ALIAS;
-    const cudaError_t e = kqlaunch::rows(fmt, (const uint8_t *)W, rows, (int)(cols / 256), ids, n,
-                                         out, (cudaStream_t)stream);
+    // the same memory rules as kq_matvec: W in this device's memory; ids
+    // and out in device, managed or pinned host memory (read / written in
+    // place through their device addresses)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    const void *Wd = nullptr, *idsd = nullptr, *outd = nullptr;
+    bool host = false;
+    kq_status st = device_address(W, dev, false, &Wd, &host);
+    if (st == KQ_OK) st = device_address(ids, dev, true, &idsd, &host);
+    if (st == KQ_OK) st = device_address(out, dev, true, &outd, &host);
+    if (st != KQ_OK) return st;
+    e = kqlaunch::rows(fmt, (const uint8_t *)Wd, rows, (int)(cols / 256),
+                       static_cast<const int32_t *>(idsd), n,
+                       static_cast<float *>(const_cast<void *>(outd)), (cudaStream_t)stream);
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
@@ -884,7 +906,7 @@ const char *kq_status_str(int status) {
     case KQ_ERR_ALIGN: return "misaligned pointer (W, x: 16 bytes; y: 4 bytes)";
     case KQ_ERR_ALIAS: return "an output overlaps an input or another output";
     case KQ_ERR_COUNT: return "set size outside 1..16";
-    case KQ_ERR_CUDA: return "CUDA launch failed";
+    case KQ_ERR_CUDA: return "a CUDA call failed (see kq_last_cuda_error)";
     case KQ_ERR_TIMEOUT: return "device-side wait timed out";
     case KQ_ERR_LIMIT: return "inputs exceed the fixed buffer of kq_matvec_noalloc";
     case KQ_ERR_MEMORY: return "a pointer addresses memory the device cannot use there";
@@ -927,6 +949,10 @@ int kq_set_overlap(int enable) {
     return prev;
 }
 
-int kq_version(void) { return (1 << 16) | 2; }
+int kq_version(void) { return (1 << 16) | 3; }
+
+unsigned long long kq_set_wait_limit_ns(unsigned long long ns) {
+    return g_wait_ns.exchange(ns);
+}
 
 }  // extern "C"

@@ -43,7 +43,7 @@ constexpr int kMaxMaps = 4;
 constexpr int kMaxSlots = 32;
 constexpr int kOverlapPrefetch = 1;  // stages issued before the inputs (overlap)
 constexpr int kMaxHinv = 40;  // row-pair offsets hp of a stage are at most 17
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s (default)
 
 struct StreamMember {
     const uint8_t *W;
@@ -77,6 +77,7 @@ struct StreamParams {
     int32_t overlap;     // launched to overlap the preceding kernel
     uint32_t hinv[kMaxHinv + 1];  // ceil(2^20 / hp): t / hp = (t * hinv[hp]) >> 20
     unsigned int *err;   // device error word (nonzero: a wait expired)
+    unsigned long long wait_ns;  // wall-time limit of each wait
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -110,10 +111,11 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for the phase of `parity` to complete; false once the wall-time limit
-// passes.  Between polls the thread sleeps, doubling from 32 ns up to
-// `max_ns`, so that waiting warps leave the issue slots to working ones.
+// Wait for the phase of `parity` to complete; false once `limit_ns` of wall
+// time have passed.  Between polls the thread sleeps, doubling from 32 ns up
+// to `max_ns`, so that waiting warps leave the issue slots to working ones.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns,
                                           unsigned max_ns = 256) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -121,7 +123,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     while (!mbar_try(bar, parity)) {
         __nanosleep(ns);
         if (ns < max_ns) ns <<= 1;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -230,6 +232,7 @@ struct ConsumerCtx {
     int *gcount;
     const uint32_t *hinv;  // ceil(2^20 / hp) by hp
     unsigned int *err;
+    unsigned long long wait_ns;
 };
 
 template <int NTOK, bool XSMEM, int FMT>
@@ -267,7 +270,8 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
         float *pbuf = c.part_f + (g & 1) * c.part_floats;
         bool ok = !*(volatile int *)c.abort_flag;
-        if (ok && k == 0 && g >= 2 && !mbar_wait(c.xbar + 8 * (g & 1), ((g >> 1) - 1) & 1)) {
+        if (ok && k == 0 && g >= 2 &&
+            !mbar_wait(c.xbar + 8 * (g & 1), ((g >> 1) - 1) & 1, c.wait_ns)) {
             atomicExch(c.abort_flag, 1);
             atomicOr(c.err, 1u);
             ok = false;
@@ -277,7 +281,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         // the right lap (a warp that skipped it could arrive for the slot's
         // next lap before this lap's readers are done, and the producer
         // would overwrite the slot under them).
-        if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1, 128)) {
+        if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1, c.wait_ns, 128)) {
             atomicExch(c.abort_flag, 1);
             atomicOr(c.err, 1u);
             ok = false;
@@ -448,7 +452,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                 const unsigned long long t0 = global_ns();
                 while (*(volatile int *)&xissued < kStreamConsumers) {
                     __nanosleep(20);
-                    if (global_ns() - t0 > kWaitLimitNs) {
+                    if (global_ns() - t0 > p.wait_ns) {
                         atomicExch(&abort_flag, 1);
                         atomicOr(p.err, 1u);
                         break;
@@ -466,11 +470,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             int stop = 0;
             if (lane == 0) {
                 stop = *(volatile int *)&abort_flag;
-                if (!stop && s >= nslot && !mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1)) {
+                if (!stop && s >= nslot &&
+                    !mbar_wait(bars + 8 * (kMaxSlots + slot), (lap - 1) & 1, p.wait_ns)) {
                     atomicExch(&abort_flag, 1);
                     atomicOr(p.err, 1u);
                     stop = 1;
                 }
+                // Read the flag again after the slot became free: if every
+                // consumer warp gave up on this slot's last stage, they set
+                // the flag before arriving, and that stage's copy may still
+                // be landing -- the slot must not be given a second copy.
+                // (If any warp waited successfully, the copy has landed.)
+                if (!stop) stop = *(volatile int *)&abort_flag;
             }
             if (__shfl_sync(kAll, stop, 0)) break;
             const int h = (int)(g1 - g0);
@@ -536,9 +547,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         __syncwarp();
         if (lane == 0 && *(volatile int *)&abort_flag) {
             // do not leave copies in flight into this CTA's shared memory
+            // (always the default limit: copies that were issued do land)
             for (int slot = 0; slot < nslot && slot < issued; ++slot) {
                 const int last = slot + ((issued - 1 - slot) / nslot) * nslot;
-                mbar_wait(bars + 8 * slot, (last / nslot) & 1);
+                mbar_wait(bars + 8 * slot, (last / nslot) & 1, kWaitLimitNs);
             }
         }
         return;
@@ -573,6 +585,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.abort_flag = &abort_flag;
     c.gcount = gcount;
     c.err = p.err;
+    c.wait_ns = p.wait_ns;
     c.hinv = p.hinv;
     if (fmt == kFmtQ4K)
         consume<NTOK, XSMEM, kFmtQ4K>(c, warp, lane);

@@ -12,7 +12,7 @@ from quant_quantized_matvec_gb300 import build as kbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-OK, FORMAT, SHAPE, NTOK, NULL, ALIGN, ALIAS, COUNT = range(8)
+OK, FORMAT, SHAPE, NTOK, NULL, ALIGN, ALIAS, CUDA, TIMEOUT, COUNT, LIMIT, MEMORY = range(12)
 
 
 @pytest.fixture(scope="module")
@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
         if h.endswith(".h"):
             for n in header_functions(h):
                 assert hasattr(lib, n), f"{h}: {n}"
-    assert header_functions("kq_internal.h") == ["kq_plan_describe"]
+    assert header_functions("kq_internal.h") == ["kq_plan_describe", "kq_set_wait_limit_ns"]
 
 
 def test_block_and_matrix_bytes(lib):
@@ -51,9 +51,27 @@ def test_block_and_matrix_bytes(lib):
 
 
 def test_status_strings(lib):
-    for s in range(10):
-        assert lib.kq_status_str(s)
+    for s in range(12):
+        assert lib.kq_status_str(s) != b"unknown status"
     assert lib.kq_status_str(99) == b"unknown status"
+
+
+def test_status_values_follow_the_boundary(lib):
+    """The first nine codes keep the order of the boundary's enum (OK,
+    FORMAT, SHAPE, NTOK, NULL, ALIGN, ALIAS, CUDA, TIMEOUT); the library's
+    extra codes come after them.  Read from the header text itself."""
+    with open(os.path.join(ROOT, "include", "kq.h")) as f:
+        src = f.read()
+    vals = dict((k, int(v)) for k, v in re.findall(r"\b(KQ_[A-Z_]+) = (\d+)", src))
+    assert [vals[k] for k in ("KQ_OK", "KQ_ERR_FORMAT", "KQ_ERR_SHAPE", "KQ_ERR_NTOK",
+                              "KQ_ERR_NULL", "KQ_ERR_ALIGN", "KQ_ERR_ALIAS",
+                              "KQ_ERR_CUDA", "KQ_ERR_TIMEOUT")] == list(range(9))
+    assert (vals["KQ_ERR_COUNT"], vals["KQ_ERR_LIMIT"], vals["KQ_ERR_MEMORY"]) == (9, 10, 11)
+    for k, v in vals.items():
+        if k.startswith("KQ_ERR_") or k == "KQ_OK":
+            assert _binding.STATUS[v] == k
+    assert lib.kq_status_str(CUDA).decode().startswith("a CUDA call")
+    assert lib.kq_status_str(TIMEOUT).decode().startswith("device-side wait")
 
 
 # fake, well-aligned device addresses: validation must reject the call

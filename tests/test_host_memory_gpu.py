@@ -163,3 +163,41 @@ def test_refuses_memory_the_device_cannot_address():
     assert (pageable_y == 5.0).all()
     assert (yd.host() == 2.0).all()
     assert lib.kq_status_str(KQ_ERR_MEMORY).decode().startswith("a pointer")
+
+
+def test_dequant_rows_refuses_memory_the_device_cannot_address():
+    """kq_dequant_rows checks its pointers like kq_matvec: pageable host ids
+    or out, and W outside device memory, return KQ_ERR_MEMORY through the C
+    ABI with nothing launched; pinned host ids and out are used in place."""
+    lib = _binding.load()
+    fmt, rows, cols, n = kq.Q4_K, 64, 512, 3
+    W, _ = C.case(fmt, rows, cols, 1, "host/rows")
+    Wd = C.to_dev(W)
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ids_np = np.array([5, 0, 63], dtype=np.int32)
+    ids_d = torch.from_numpy(ids_np).cuda()
+    out_d = torch.full((n, cols), 2.0, dtype=torch.float32, device="cuda")
+    pageable_out = np.full((n, cols), 5.0, dtype=np.float32)
+    assert pageable_out.ctypes.data % 16 == 0
+    Wh = torch.from_numpy(W.reshape(-1)).pin_memory()
+    calls = [
+        (Wd.data_ptr(), ids_np.ctypes.data, out_d.data_ptr()),
+        (Wd.data_ptr(), ids_d.data_ptr(), pageable_out.ctypes.data),
+        (Wh.data_ptr(), ids_d.data_ptr(), out_d.data_ptr()),
+    ]
+    for w, ip, op in calls:
+        assert lib.kq_dequant_rows(fmt, ctypes.c_void_p(w), rows, cols, ctypes.c_void_p(ip),
+                                   n, ctypes.c_void_p(op), s) == KQ_ERR_MEMORY
+    torch.cuda.synchronize()
+    assert (pageable_out == 5.0).all()
+    assert bool((out_d == 2.0).all())
+    # pinned host ids and out: gathered in place, bit for bit the oracle's rows
+    ids_h = torch.from_numpy(ids_np).pin_memory()
+    out_h = torch.empty((n, cols), dtype=torch.float32).pin_memory()
+    assert lib.kq_dequant_rows(fmt, ctypes.c_void_p(Wd.data_ptr()), rows, cols,
+                               ctypes.c_void_p(ids_h.data_ptr()), n,
+                               ctypes.c_void_p(out_h.data_ptr()), s) == 0
+    torch.cuda.synchronize()
+    import oracle
+    ref = oracle.dequant_rows(fmt, W, cols, rows=ids_np.tolist())
+    assert np.array_equal(out_h.numpy().view(np.uint32), ref.view(np.uint32))

@@ -1,6 +1,14 @@
-"""kq_matvec_noalloc through the C ABI: two calls in a row on the one fixed
-record buffer, each compared with kq_matvec on the same inputs at the
-contract tolerance (and with the oracle), plus its size limit.
+"""kq_matvec_noalloc through the C ABI.
+
+Some callers cannot allocate device memory during a call: code running under
+an allocator or a memory budget that forbids hidden allocations, and loops
+that must not take an allocator's locks.  kq_matvec_noalloc serves them with
+the direct-load kernel and one fixed device buffer for its input records.
+Its results must be bitwise those of kq_matvec with the direct-load kernel
+selected, on two calls in a row that reuse the buffer, on a call that runs
+as two launches in turn on the buffer (ntok = 12), and with x in pinned host
+memory (read in place, since staging would allocate); each is also checked
+against the oracle.  Calls beyond the buffer are refused.
 
 Collected last on purpose (file name) and self-contained, so it passes both
 alone in a fresh process -- where its first call sets the buffer up -- and
@@ -21,50 +29,74 @@ from quant_quantized_matvec_gb300 import _binding  # noqa: E402
 
 KQ_OK, KQ_ERR_LIMIT = 0, 10
 NOALLOC_RECORD_BYTES = 1 << 20
+DIRECT = 1  # kq_select_kernel: always the direct-load kernel
 
 
 def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def _call(fn, fmt, Wd, rows, cols, xd, y, ntok):
+def _call(fn, fmt, Wd, rows, cols, xp, y, ntok):
     return fn(fmt, ctypes.c_void_p(Wd.data_ptr()), rows, cols,
-              ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(y.data_ptr()),
+              ctypes.c_void_p(xp.data_ptr()), ctypes.c_void_p(y.data_ptr()),
               ntok, _stream())
 
 
-def test_noalloc_two_calls_match_kq_matvec():
+def _direct_reference(lib, fmt, Wd, rows, cols, xd, ntok):
+    """kq_matvec's output with the direct-load kernel selected."""
+    prev = lib.kq_select_kernel(DIRECT)
+    try:
+        ref = C.Guarded(ntok, rows)
+        assert _call(lib.kq_matvec, fmt, Wd, rows, cols, xd, ref.y, ntok) == KQ_OK
+        torch.cuda.synchronize()
+        return ref.host()
+    finally:
+        lib.kq_select_kernel(prev)
+
+
+CASES = [(kq.Q6_K, 300, 6656, 2, "noalloc/a"),
+         (kq.Q4_K, 517, 2816, 5, "noalloc/b"),
+         (kq.Q5_K, 133, 1536, 12, "noalloc/c")]
+
+
+def test_noalloc_calls_in_a_row_bitwise_equal_direct_kq_matvec():
     lib = _binding.load()
-    cases = [(kq.Q6_K, 300, 6656, 2, "noalloc/a"),
-             (kq.Q4_K, 517, 2816, 5, "noalloc/b")]
     inputs = []
-    for fmt, rows, cols, ntok, label in cases:
+    for fmt, rows, cols, ntok, label in CASES:
         W, x = C.case(fmt, rows, cols, ntok, label)
         inputs.append((fmt, rows, cols, ntok, W, x, C.to_dev(W), C.to_dev(x)))
-    # two no-allocation calls back to back on the shared buffer
-    outs = []
-    for fmt, rows, cols, ntok, W, x, Wd, xd in inputs:
-        g = C.Guarded(ntok, rows)
-        assert _call(lib.kq_matvec_noalloc, fmt, Wd, rows, cols, xd, g.y,
-                     ntok) == KQ_OK
-        outs.append(g)
-    torch.cuda.synchronize()
-    for (fmt, rows, cols, ntok, W, x, Wd, xd), g in zip(inputs, outs):
-        ref = C.Guarded(ntok, rows)
-        assert _call(lib.kq_matvec, fmt, Wd, rows, cols, xd, ref.y,
-                     ntok) == KQ_OK
+    # the no-allocation calls back to back on the one buffer, then again
+    for rep in range(2):
+        outs = []
+        for fmt, rows, cols, ntok, W, x, Wd, xd in inputs:
+            g = C.Guarded(ntok, rows)
+            assert _call(lib.kq_matvec_noalloc, fmt, Wd, rows, cols, xd, g.y, ntok) == KQ_OK
+            # ntok = 12 runs as two launches of the record pass and the kernel
+            assert lib.kq_last_launch_count() == (4 if ntok > 8 else 2)
+            outs.append(g)
         torch.cuda.synchronize()
-        y_na, y_mv = g.host(), ref.host()
-        _, S = kq_oracle_S(fmt, W, rows, cols, x)
-        assert np.all(np.abs(y_na.astype(np.float64) - y_mv) <=
-                      C.REL_TOL * S + C.ABS_TOL)
-        C.check(fmt, W, rows, cols, x, y_na, what="kq_matvec_noalloc")
+        for (fmt, rows, cols, ntok, W, x, Wd, xd), g in zip(inputs, outs):
+            y_na = g.host()
+            y_mv = _direct_reference(lib, fmt, Wd, rows, cols, xd, ntok)
+            assert np.array_equal(y_na.view(np.uint32), y_mv.view(np.uint32)), (rep, fmt)
+            C.check(fmt, W, rows, cols, x, y_na, what=f"kq_matvec_noalloc call {rep}")
     assert not kq.device_error()
 
 
-def kq_oracle_S(fmt, W, rows, cols, x):
-    import oracle
-    return oracle.matvec(fmt, W, rows, cols, x)
+def test_noalloc_reads_pinned_host_x_in_place():
+    lib = _binding.load()
+    fmt, rows, cols, ntok = kq.Q4_K, 250, 2560, 3
+    W, x = C.case(fmt, rows, cols, ntok, "noalloc/host")
+    Wd, xd = C.to_dev(W), C.to_dev(x)
+    xh = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    g = C.Guarded(ntok, rows)
+    assert _call(lib.kq_matvec_noalloc, fmt, Wd, rows, cols, xh, g.y, ntok) == KQ_OK
+    torch.cuda.synchronize()
+    y_na = g.host()
+    y_mv = _direct_reference(lib, fmt, Wd, rows, cols, xd, ntok)
+    assert np.array_equal(y_na.view(np.uint32), y_mv.view(np.uint32))
+    C.check(fmt, W, rows, cols, x, y_na, what="kq_matvec_noalloc, host x")
+    assert not kq.device_error()
 
 
 def test_noalloc_rejects_records_beyond_its_buffer():
