@@ -160,6 +160,13 @@ def recorded_traffic(workload_name, ntok):
     return None
 
 
+def props_clock_hz(props) -> float:
+    """SM clock for converting a sleep length to cycles (the maximum clock,
+    so a sleep is at least as long as asked)."""
+    mhz = getattr(props, "clock_rate", 0) / 1e3 if getattr(props, "clock_rate", 0) else 2070.0
+    return max(mhz, 2070.0) * 1e6
+
+
 def max_over_ranks(value, dist, device=None):
     """The largest of every rank's value (a job takes as long as its slowest
     rank); `value` itself when the run is not distributed."""
@@ -359,11 +366,20 @@ def run_ours(args, rank, world, dist):
 
     K = args.steps
     L = min(K, args.graph_len)
+    head_cycles = int(args.head_start_ms * 1e-3 * props_clock_hz(props))
 
     def timed(overlap, sampler=None, stepfn=step, K=K):
         """K steps replayed from CUDA graphs of L steps, captured with the
         given launch-overlap setting; -> ms (max over ranks), wall s,
-        (replays, remainder steps), µs per call of each main-graph replay."""
+        (replays, remainder steps), µs per call of each main-graph replay,
+        pre-warm ms.
+
+        Steady state: before the timed region the main graph is replayed,
+        untimed, for at least --prewarm-ms of wall time (clocks and caches
+        settle, the launch path is warm), and a GPU sleep of --head-start-ms
+        is queued just before the start event, so that the host has queued
+        every timed replay before the GPU reaches that event: the timed
+        region holds exactly K calls and no host launch gap."""
         kq.set_overlap(overlap)
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
@@ -381,9 +397,17 @@ def run_ours(args, rank, world, dist):
         g_main = capture(L)
         reps, rem = K // L, K % L
         g_rem = capture(rem) if rem else None
-        with torch.cuda.stream(stream):
-            g_main.replay()  # untimed warm replay of the graph itself
         torch.cuda.synchronize()
+        t_pre = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while True:
+                g_main.replay()
+                if g_rem is not None:
+                    g_rem.replay()
+                torch.cuda.synchronize()
+                if time.perf_counter() - t_pre >= args.prewarm_ms * 1e-3:
+                    break
+        prewarm_ms = (time.perf_counter() - t_pre) * 1e3
         if sampler:
             sampler.start()
             time.sleep(0.3)
@@ -396,6 +420,8 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(head_cycles)  # outside the timed region
         ev0.record(stream)
         with torch.cuda.stream(stream):
             for r in range(reps):
@@ -411,7 +437,7 @@ def run_ours(args, rank, world, dist):
         ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
         per_replay = [ev0.elapsed_time(evs[0])] + [
             evs[r - 1].elapsed_time(evs[r]) for r in range(1, reps)]
-        return ms, wall, (reps, rem), [1e3 * t / L for t in per_replay]
+        return ms, wall, (reps, rem), [1e3 * t / L for t in per_replay], prewarm_ms
 
     overlap = not args.no_overlap
     ms_serial = timed(False)[0]
@@ -420,7 +446,7 @@ def run_ours(args, rank, world, dist):
     ms_warm = (timed(overlap, stepfn=lambda i: step(0), K=Kw)[0]
                if copies > 1 else None)
     sampler = ClockSampler(dev.index)
-    ms, wall, (reps, rem), per_replay = timed(overlap, sampler)
+    ms, wall, (reps, rem), per_replay, prewarm_ms = timed(overlap, sampler)
     per_replay = sorted(per_replay)
     clocks = sampler.stop()
     kernels = kq.last_kernels()
@@ -450,6 +476,13 @@ def run_ours(args, rank, world, dist):
     kq.set_overlap(overlap)
 
     def e2e(host_y):
+        """Ke steps through the public API, timed on the device; the host
+        cost of issuing one step is measured separately, on the warm-up
+        steps (wall clock of their loop, which never waits for the GPU).  A GPU sleep queued before the start
+        event gives the host a head start of about the whole loop's issue
+        time, so that the device timeline is the one a caller gets when it
+        keeps the stream fed (as a serving loop or a captured graph does);
+        -> (device ms, host µs per step)."""
         def one(i):
             if host_y:
                 mem, d = host_sets[i % len(host_sets)]
@@ -459,26 +492,32 @@ def run_ours(args, rank, world, dist):
                     xd[p].copy_(x_host[p], non_blocking=True)
                 step(i)
                 y_host.copy_(y_all, non_blocking=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         with torch.cuda.stream(stream):
-            for i in range(3):
+            for i in range(max(3, args.warmup)):
                 one(i)
+        host_us = (time.perf_counter() - t0) * 1e6 / max(3, args.warmup)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
+        lead_ms = min(200.0, 1.5 * host_us * Ke * 1e-3 + args.head_start_ms)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(lead_ms * 1e-3 * props_clock_hz(props)))
         e0.record(stream)
         with torch.cuda.stream(stream):
             for i in range(Ke):
                 one(i)
         e1.record(stream)
         torch.cuda.synchronize()
-        return max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        return max_over_ranks(e0.elapsed_time(e1), dist, dev), host_us
 
-    ems = e2e(True)
+    ems, host_us = e2e(True)
     y_direct = y_host.clone()
-    ems_copy = e2e(False)
+    ems_copy, host_us_copy = e2e(False)
     # the last step wrote the same outputs both ways
     e2e_same = bool(torch.equal(y_direct.view(torch.int32), y_host.view(torch.int32)))
     e2e_gbs = job_gbs(step_bytes, Ke, world, ems)
@@ -511,6 +550,8 @@ def run_ours(args, rank, world, dist):
                    f"weights {w_bytes / 1e6:.0f} MB > 3x L2"),
             "timing": f"CUDA graphs of {L} calls, {reps} replays"
                       + (f" + {rem}" if rem else "") + ", events on stream"
+                      + f"; untimed pre-warm of {prewarm_ms:.0f} ms of replays and a "
+                        f"{args.head_start_ms:g} ms GPU head start before the timed region"
                       + ("; launch overlap on: a call's weights stream "
                          "while the previous call finishes, its x is read "
                          "after that call completes" if overlap else ""),
@@ -523,6 +564,7 @@ def run_ours(args, rank, world, dist):
                     "max_us_per_call": round(per_replay[-1], 3),
                     "note": "per replay of the main graph inside the timed region (this rank)"},
         "launch_overlap": overlap,
+        "prewarm_ms": round(prewarm_ms, 1),
         "warm_l2": ({"us_per_call": round(ms_warm * 1e3 / Kw, 3),
                      "value": round(job_gbs(step_bytes, Kw, world, ms_warm), 2),
                      "note": "warm, L2-resident: one weight copy reused every call "
@@ -546,6 +588,10 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(ems * 1e3 / Ke, 3), "steps": Ke,
+                "host_us_per_step": round(host_us, 3),
+                "timing": "device time (CUDA events on the stream) of Ke calls "
+                          "queued back to back; host_us_per_step is the host's "
+                          "cost of issuing one call (Python + C ABI + launches)",
                 "weights": "resident in HBM",
                 "path": "x and y in pinned host memory, passed to the call: the "
                         "library copies x to the device with a staging kernel that "
@@ -554,6 +600,7 @@ def run_ours(args, rank, world, dist):
                 "outputs_equal_copy_path": e2e_same,
                 "copy_path": {"value": round(job_gbs(step_bytes, Ke, world, ems_copy), 2),
                               "us_per_step": round(ems_copy * 1e3 / Ke, 3),
+                              "host_us_per_step": round(host_us_copy, 3),
                               "path": "x and y in device memory, with async copies "
                                       "from and to pinned host memory around each call"}},
         "clocks": clocks,
@@ -614,6 +661,11 @@ def run_embed(args, rank, world, dist):
     with torch.cuda.stream(stream):
         g.replay()
     torch.cuda.synchronize()
+    t_pre = time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t_pre < args.prewarm_ms * 1e-3:
+            g.replay()
+            torch.cuda.synchronize()
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
@@ -622,6 +674,9 @@ def run_embed(args, rank, world, dist):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(args.head_start_ms * 1e-3 * props_clock_hz(props)))
     e0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(reps):
@@ -697,17 +752,18 @@ def run_embed(args, rank, world, dist):
 
 # ----------------------------------------------------------------- reference
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step evaluates a bounded row
-    sample of the workload (rows cycle through every matrix)."""
+    """The CPU oracle as the reference arm: each step is one pass of the
+    oracle over the whole workload, as cpu_baseline times it (a matrix above
+    64 MB contributes 2048 rows drawn afresh every step, so that the sample
+    does not stay in the host's caches)."""
     import oracle
     oracle.build()
     members, desc = workload(args.workload, args.ntok)
     ntok = args.ntok
     Ws, planes = host_inputs(members, ntok, f"bench/{args.workload}")
-    rows_per_step = args.ref_rows_per_step
-    cursor = [0] * len(members)
     embed = args.workload == "embed_q4k"
     rng = np.random.default_rng(1)
+    sampled = []
 
     def step():
         if embed:  # the lookup itself: ntok random rows per step
@@ -716,11 +772,15 @@ def run_reference(args):
             return ntok * ((c // 256) * synth.BLOCK_BYTES[f] + 4 + 4 * c)
         nbytes = 0
         for i, (f, r, c, p) in enumerate(members):
-            idx = (cursor[i] + np.arange(rows_per_step)) % r
-            cursor[i] = int((cursor[i] + rows_per_step) % r)
-            oracle.matvec(f, Ws[i], r, c, planes[p], row_idx=idx)
-            nbytes += len(idx) * (c // 256) * synth.BLOCK_BYTES[f] + \
-                4 * ntok * (c + len(idx))
+            bpr = (c // 256) * synth.BLOCK_BYTES[f]
+            if r * bpr > 64 << 20:
+                idx = np.sort(rng.choice(r, size=2048, replace=False))
+                oracle.matvec(f, Ws[i], r, c, planes[p], row_idx=idx)
+                nbytes += len(idx) * bpr + 4 * ntok * (c + len(idx))
+                sampled.append(i)
+            else:
+                oracle.matvec(f, Ws[i], r, c, planes[p])
+                nbytes += r * bpr + 4 * ntok * (c + r)
         return nbytes
 
     for _ in range(args.warmup):
@@ -731,8 +791,10 @@ def run_reference(args):
         total += step()
     el = time.perf_counter() - t0
     gbs = total / el / 1e9
-    sample = (f"{rows_per_step} consecutive rows of each matrix per step, "
-              f"single-threaded oracle (f32 dequant + f64 dots)")
+    sample = ("ntok random token rows per step" if embed else
+              "one pass over every matrix of the workload per step"
+              + (" (2048 fresh random rows of each matrix above 64 MB)" if sampled else "")) \
+        + f", {el:.1f} s single-threaded oracle (f32 dequant + f64 dots)"
     return {
         "metric": METRIC, "impl": "reference",
         "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1,
@@ -759,11 +821,14 @@ def main():
     ap.add_argument("--ntok", type=int, default=1)
     ap.add_argument("--graph-len", type=int, default=2000)
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--prewarm-ms", type=float, default=300.0,
+                    help="untimed replays of the main graph before each timed region")
+    ap.add_argument("--head-start-ms", type=float, default=2.0,
+                    help="GPU sleep queued before the start event (host head start)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
                     help="headline with launch overlap off")
-    ap.add_argument("--ref-rows-per-step", type=int, default=1)
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
