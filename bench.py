@@ -25,13 +25,16 @@ minimum and maximum us per call over the graph replays of the timed region.
 `e2e` times the public Python API with x and y in pinned host memory: each
 call copies its x in and writes its y back inside the timed region (weights
 stay resident, as model weights do); the same steps with explicit copies
-around device buffers are reported beside it.  `cpu_baseline` times the CPU
+around device buffers are reported beside it.  Timed regions are preceded by
+an untimed pre-warm (--prewarm-ms of graph replays) and a GPU sleep
+(--head-start-ms), so that they measure steady state and not the host's
+launch gap.  `cpu_baseline` times the CPU
 oracle on a bounded sample, single-threaded and (`all_cores`) with the rows
 split over every host core.
 
---impl reference times the CPU oracle itself (single thread) on a bounded
-sample of the same workload each step, and prints the same JSON line with
-"impl": "reference".
+--impl reference times the CPU oracle itself (single thread), one pass over
+the workload's matrices per step (2048 fresh random rows of any matrix above
+64 MB), and prints the same JSON line with "impl": "reference".
 """
 from __future__ import annotations
 
@@ -492,6 +495,8 @@ def run_ours(args, rank, world, dist):
                     xd[p].copy_(x_host[p], non_blocking=True)
                 step(i)
                 y_host.copy_(y_all, non_blocking=True)
+        with torch.cuda.stream(stream):
+            one(0)  # first call: one-time set-up (pointer lookups, tensor maps)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
