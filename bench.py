@@ -587,7 +587,8 @@ def run_ours(args, rank, world, dist):
             "traffic": traffic,
             "peak_source": f"{peak_kind} HBM copy bandwidth",
             "frac_of_nominal": round(step_bytes / (ms * 1e-3 / K) / 1e9 / NOMINAL_HBM_GBS, 4),
-            "kernel": "kq_set_stream" if kernels["stream"] else "kq_set_direct",
+            "kernel": ("kq_set_stream" if kernels["stream"] else "kq_set_direct")
+                      + (" (tensor cores, after the fragment pass)" if kernels.get("tensor_cores") else ""),
             "launches_per_step": launches_per_step,
         },
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s",

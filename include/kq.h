@@ -13,12 +13,14 @@
  *     Q5_K  176 B / block   w = d*sc_j*(nibble | hbit<<4) - dmin*m_j  (6.4)
  *     Q6_K  210 B / block   w = d*sc_j*(code - 32), 16 int8 scales   (6.5)
  *
- * x and y are f32.  Up to 5 token columns share one read of W; a call with
- * ntok = 6..16 runs as ceil(ntok / 5) launches over consecutive, near-equal
- * runs of token columns (6 = 3 + 3, 8 = 4 + 4, 16 = 4 + 4 + 4 + 4), each
- * reading W again -- faster than one launch, whose block sums grow with
- * the columns.  A token column's result does not depend on ntok or on the
- * other columns, so the split changes no result.
+ * x and y are f32.  A call of 1..4 token columns is one launch of the
+ * integer (dp4a) kernels, all columns sharing one read of W.  A call of
+ * 5..16 token columns runs on the tensor cores (mma.sync m16n8k16, f16
+ * operands, f32 accumulation; "Chapter 6", section 6.8, the weight-
+ * stationary tile for many columns): a short pass turns x into f16 operand
+ * fragments, then one launch reads W once for all the columns.  A token
+ * column's result depends on its own inputs and on which of the two
+ * arithmetics the call's ntok selects -- never on the other columns.
  *
  * Conventions for every entry point below
  *   - W is a DEVICE pointer (cudaMalloc / torch CUDA storage on the current
@@ -35,14 +37,17 @@
  *     keeps no pointer after a call returns and never synchronizes.  Its
  *     allocations are stream-ordered temporaries (cudaMallocAsync /
  *     cudaFreeAsync on `stream`): the input records of calls whose records
- *     do not fit in shared memory, and staged host inputs;
- *     kq_matvec_noalloc allocates nothing.
+ *     do not fit in shared memory, the tensor-core fragments of calls of 5
+ *     or more token columns (about 8 KB per 256 inputs per group of 8
+ *     columns), and staged host inputs; kq_matvec_noalloc allocates
+ *     nothing.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream) and may be captured in a CUDA graph.
  *   - Every argument is validated on the host before anything is launched;
  *     a call that returns an error has enqueued nothing, with one exception:
- *     KQ_ERR_CUDA from a later launch of a call that runs as several
- *     (ntok > 5), after the earlier ones had been enqueued.  KQ_ERR_CUDA means a launch itself failed;
+ *     KQ_ERR_CUDA from a later launch of a call that runs as several (the
+ *     staging, fragment or record pass and the matvec), after the earlier
+ *     ones had been enqueued.  KQ_ERR_CUDA means a launch itself failed;
  *     kq_last_cuda_error() returns the CUDA error code of the most recent
  *     such failure on the calling thread.
  *   - Results are deterministic: a row's arithmetic depends only on the
@@ -62,7 +67,16 @@
  *     hundreds of times inside it; an input of 1e6 on an exactly zero
  *     weight among N(0,1) inputs is about 10x outside it, though still
  *     within B.  NaN or infinite inputs make the outputs that read their
- *     group NaN.
+ *     group NaN.  This holds for calls of 1..4 token columns.
+ *     Calls of 5..16 token columns (tensor cores) hold each input as two f16
+ *     terms after scaling its 256-input column by a power of two: an input
+ *     error of at most max(2^-22 |x_j|, 2^(E-39)), max|x| < 2^E over the
+ *     column; codes times these terms are exact and the sums are f32.  The
+ *     same contract holds there with the precondition relaxed to inputs up
+ *     to about 10^7 times their column's typical magnitude on a zero
+ *     weight.  On both paths a row whose weights are all exactly zero gives
+ *     exactly zero.  NaN or infinite inputs make the outputs that read their
+ *     256-input column NaN.
  */
 #ifndef KQ_H
 #define KQ_H
@@ -253,7 +267,9 @@ int kq_set_overlap(int enable);
  * Kernels the calling thread's most recent successful kq_matvec /
  * kq_matvec_set / kq_matvec_noalloc call enqueued, as bits: 1 = the direct-load kernel, 2 = the
  * TMA-streaming kernel, 4 = the pass that writes input records to global
- * memory first (when they do not fit in shared memory).  0 before any call.
+ * memory first (when they do not fit in shared memory), 8 = the tensor-core
+ * arithmetic (calls of 5 or more token columns, after their fragment pass).
+ * 0 before any call.
  */
 int kq_last_kernels(void);
 
@@ -277,12 +293,13 @@ int kq_last_launch_count(void);
  * Same arguments, result and errors as kq_matvec, computed by the direct-
  * load kernel with its input records (see the record pass) in one fixed
  * file-scope device buffer of KQ_NOALLOC_RECORD_BYTES bytes instead of a
- * stream-ordered temporary.  Calls whose records need more -- min(ntok, 8)
- * * (cols / 256) * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K (the
- * records of one launch; ntok > 8 runs as two launches in stream order,
- * one after the other in the buffer) -- return KQ_ERR_LIMIT with nothing
- * enqueued.  The records are written in full before they are read, so
- * nothing in the buffer has to start at zero.
+ * stream-ordered temporary.  Calls whose records need more return
+ * KQ_ERR_LIMIT with nothing enqueued: for ntok = 1..4, ntok * (cols / 256)
+ * * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K; for ntok = 5..16
+ * (tensor cores), ceil(ntok / 8) * (cols / 256) * 8192 bytes of fragments
+ * plus ntok * (cols / 256) * 64 bytes, each plane rounded up to 256 bytes.
+ * The records are written in full before they are read, so nothing in the
+ * buffer has to start at zero.
  *
  * The first call on a device looks the buffer up (cudaGetSymbolAddress,
  * once per device); make that first call before any stream capture.  Every

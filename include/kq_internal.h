@@ -15,12 +15,13 @@ extern "C" {
 
 /* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
  * KQ_PLAN_MEMBER per member. */
-#define KQ_PLAN_HEAD 10
+#define KQ_PLAN_HEAD 11
 #define KQ_PLAN_MEMBER 20
 
 /*
  * The streaming kernel's launch geometry for the set `mats` (n members,
- * ntok 1..8 token columns in the launch) on a device with `sms` SMs and
+ * ntok token columns in the launch: 1..3 for the dp4a kernels, 4..16 for
+ * the tensor-core kernels, as the library chooses) on a device with `sms` SMs and
  * `smem_optin` bytes of opt-in shared memory per CTA, as the library would
  * plan it.  Pure host arithmetic on the descriptors' shapes and formats
  * (their pointers are not read).
@@ -30,6 +31,7 @@ extern "C" {
  *   [1] grid  [2] level (-1: records in global memory)  [3] records in
  *   shared memory (0/1)  [4] x_bytes  [5] part_bytes  [6] slot_bytes
  *   [7] nslot  [8] dynamic shared memory  [9] stages of the largest CTA
+ *   [10] bytes of the tensor-core units' scratch (0 for dp4a launches)
  *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
  *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes.
  * Returns 0, or -1 for bad arguments (nothing written).

@@ -175,10 +175,11 @@ def select_kernel(which: str) -> str:
 
 def last_kernels() -> dict:
     """Kernels enqueued by this thread's last successful call:
-    {"direct": bool, "stream": bool, "record_pass": bool}."""
+    {"direct": bool, "stream": bool, "record_pass": bool,
+    "tensor_cores": bool}."""
     b = _lib().kq_last_kernels()
     return {"direct": bool(b & 1), "stream": bool(b & 2),
-            "record_pass": bool(b & 4)}
+            "record_pass": bool(b & 4), "tensor_cores": bool(b & 8)}
 
 
 def last_launch_count() -> int:

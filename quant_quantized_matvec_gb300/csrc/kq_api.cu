@@ -106,6 +106,41 @@ __global__ void __launch_bounds__(kStageThreads) kq_xstage(const __grid_constant
     p.dst[k][o] = p.src[k][o];
 }
 
+// Input fragments of the tensor-core launches (kq_xtc.cuh): kTcPrepSplit
+// warps per (plane, octet, column); planes are the distinct (x, cols) of a
+// set.
+struct TcPrepParams {
+    const float *x[KQ_MAX_SET];
+    uint8_t *frag[KQ_MAX_SET];
+    float *aux[KQ_MAX_SET];
+    int32_t nb[KQ_MAX_SET];
+    int64_t first_warp[KQ_MAX_SET + 1];
+    int32_t n, ntok;
+};
+constexpr int kTcPrepThreads = 128;
+
+__global__ void __launch_bounds__(kTcPrepThreads) kq_xprep_tc(const __grid_constant__ TcPrepParams p) {
+    // the matvec launched after this pass overlaps it (streaming its
+    // weights) and waits for it before reading the fragments; this pass,
+    // when launched to overlap the kernel before it, waits for that kernel
+    // before reading x (a no-op otherwise)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t w = ((int64_t)blockIdx.x * kTcPrepThreads + threadIdx.x) >> 5;
+    if (w >= p.first_warp[p.n]) return;
+    int k = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.n; ++i)
+        if (w >= p.first_warp[i]) k = i;
+    const int i = (int)(w - p.first_warp[k]);
+    const int nb = p.nb[k];
+    const int q = i % kTcPrepSplit, oj = i / kTcPrepSplit;
+    const int o = oj / nb, j = oj - o * nb;
+    build_tc_record(p.x[k], p.ntok, nb, o, j, q,
+                    p.frag[k] + ((int64_t)o * nb + j) * kTcFragColBytes, p.aux[k],
+                    threadIdx.x & 31);
+}
+
 }  // namespace kq
 
 namespace {
@@ -528,6 +563,214 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     return KQ_OK;
 }
 
+// ------------------------------------------------------- tensor-core path
+// Calls of kq::kTcMinNtok or more token columns (at most 16) run as one
+// tensor-core launch (kq_tc.cuh): one pass builds the input fragments of
+// each distinct input plane into global memory (kq_xprep_tc), and the
+// streaming (or direct-load) kernel reads W once for all the columns.
+// KQ_TC=off keeps such calls on the dp4a kernels (measurement only).
+int tc_enabled() {
+    static std::atomic<int> v{-1};
+    int c = v.load();
+    if (c < 0) {
+        const char *e = getenv("KQ_TC");
+        c = (e && !strcmp(e, "off")) ? 0 : 1;
+        v.store(c);
+    }
+    return c;
+}
+
+// Fragments of every member in `buf` (caller-provided, or a stream-ordered
+// temporary when buf is null: *owned is then set).  frag[i] / aux[i]:
+// member i's fragments and aux array.
+int64_t tc_records_bytes(const kq_mat *mats, int n, int ntok) {
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        bool seen = false;
+        for (int j = 0; j < i && !seen; ++j)
+            seen = mats[j].x == mats[i].x && mats[j].cols == mats[i].cols;
+        if (!seen) total += (kq::tc_record_bytes(ntok, (int)(mats[i].cols / 256)) + 255) / 256 * 256;
+    }
+    return total;
+}
+
+cudaError_t prepare_tc_records(const kq_mat *mats, int n, int ntok, cudaStream_t s, uint8_t *buf,
+                               uint8_t **owned, const uint8_t **frag, const float **aux) {
+    *owned = nullptr;
+    const int64_t total = tc_records_bytes(mats, n, ntok);
+    if (!buf) {
+        const cudaError_t e = cudaMallocAsync((void **)&buf, (size_t)total, s);
+        if (e != cudaSuccess) return e;
+        *owned = buf;
+    }
+    kq::TcPrepParams p{};
+    p.ntok = ntok;
+    const int noct = (ntok + 7) / 8;
+    int plane_of[KQ_MAX_SET];
+    int64_t off = 0, warps = 0;
+    for (int i = 0; i < n; ++i) {
+        plane_of[i] = -1;
+        for (int k = 0; k < p.n && plane_of[i] < 0; ++k)
+            if (p.x[k] == mats[i].x && p.nb[k] == (int)(mats[i].cols / 256)) plane_of[i] = k;
+        if (plane_of[i] < 0) {
+            const int k = p.n++;
+            const int nb = (int)(mats[i].cols / 256);
+            p.x[k] = mats[i].x;
+            p.nb[k] = nb;
+            p.frag[k] = buf + off;
+            p.aux[k] = reinterpret_cast<float *>(buf + off + kq::tc_frag_bytes(noct, nb));
+            off += (kq::tc_record_bytes(ntok, nb) + 255) / 256 * 256;
+            p.first_warp[k] = warps;
+            warps += (int64_t)noct * nb * kq::kTcPrepSplit;
+            plane_of[i] = k;
+        }
+        frag[i] = p.frag[plane_of[i]];
+        aux[i] = p.aux[plane_of[i]];
+    }
+    p.first_warp[p.n] = warps;
+    const int64_t blocks = (warps * 32 + kq::kTcPrepThreads - 1) / kq::kTcPrepThreads;
+    // With launch overlap on, the pass is scheduled while the kernel before
+    // it still runs and waits for it on the GPU (it writes nothing before
+    // that wait), so the launch latency is hidden.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kq::kTcPrepThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (g_overlap.load()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kq::kq_xprep_tc, p);
+    if (e != cudaSuccess && *owned) {
+        cudaFreeAsync(*owned, s);
+        *owned = nullptr;
+    }
+    return e;
+}
+
+// Rows per CTA of the direct-load kernel in a tensor-core launch: one
+// 16-row tile, fewer when the matrix would not reach every SM or the
+// partials would not fit; 0 if not even one row fits.
+int64_t direct_tc_rows_per_cta(const kq_mat &m, int ntok, int sms) {
+    const int nb = (int)(m.cols / 256);
+    const int nt = 8 * ((ntok + 7) / 8);
+    int64_t rpc = std::min<int64_t>(16, std::max<int64_t>(1, (m.rows + sms - 1) / sms));
+    while (rpc > 0 && kq::direct_smem_bytes(nb, (int)rpc, nt, true) > kSmemLimit) --rpc;
+    return rpc;
+}
+
+kq_status run_direct_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
+                        const DeviceInfo &info, const uint8_t *const *frag,
+                        const float *const *aux) {
+    kq::SetParams p{};
+    p.n = n;
+    p.ntok = ntok;
+    const int noct = (ntok + 7) / 8;
+    int64_t grid = 0;
+    size_t smem = 0;
+    for (int i = 0; i < n; ++i) {
+        const kq_mat &m = mats[i];
+        const int nb = (int)(m.cols / 256);
+        const int64_t rpc = direct_tc_rows_per_cta(m, ntok, info.sms);
+        if (rpc < 1) return KQ_ERR_SHAPE;
+        p.m[i].W = (const uint8_t *)m.W;
+        p.m[i].x = m.x;
+        p.m[i].rec = frag[i];
+        p.m[i].tc_aux = aux[i];
+        p.m[i].y = m.y;
+        p.m[i].rows = m.rows;
+        p.m[i].nb = nb;
+        p.m[i].fmt = m.fmt;
+        p.m[i].cta_begin = (int32_t)grid;
+        p.m[i].rpc = (int32_t)rpc;
+        grid += (m.rows + rpc - 1) / rpc;
+        smem = std::max<size_t>(smem, (size_t)kq::direct_smem_bytes(nb, (int)rpc, 8 * noct, true));
+        if (grid > 0x7FFFFFFF) return KQ_ERR_SHAPE;
+    }
+    const cudaError_t e = kqlaunch::direct_tc(noct, p, (int)grid, smem, s);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    g_last_kernels = 1 | 4 | 8;
+    g_last_launches = 2;
+    return KQ_OK;
+}
+
+kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
+                        const DeviceInfo &info, const uint8_t *const *frag,
+                        const float *const *aux, bool *launched) {
+    *launched = false;
+    static kq::StreamParams p;  // ~10 KB: kept off the stack
+    static std::mutex pmu;
+    std::lock_guard<std::mutex> plock(pmu);
+    memset(&p, 0, sizeof(p));
+    p.n = n;
+    const int noct = (ntok + 7) / 8;
+    kqplan::Plan P;
+    const kq_status ps = kqplan::plan_stream(mats, n, ntok, info.sms, info.smem_optin, &P, noct);
+    if (ps != KQ_OK) return ps;
+    for (int i = 0; i < n; ++i) {
+        const kq_mat &m = mats[i];
+        const kqplan::Member &Q = P.m[i];
+        kq::StreamMember &M = p.m[i];
+        M.W = (const uint8_t *)m.W;
+        M.x = m.x;
+        M.rec = frag[i];
+        M.tc_aux = aux[i];
+        M.y = m.y;
+        M.rows = m.rows;
+        M.nb = (int)(m.cols / 256);
+        M.fmt = m.fmt;
+        M.cta_begin = Q.cta_begin;
+        M.ncta = Q.ncta;
+        M.rows_q = Q.rows_q;
+        M.rows_r = Q.rows_r;
+        for (int big = 0; big < 2; ++big) {
+            M.ng[big] = Q.ng[big];
+            M.gq[big] = Q.gq[big];
+            M.gr[big] = Q.gr[big];
+        }
+        M.rmax = Q.rmax;
+        M.kb = Q.kb;
+        M.seg = Q.seg;
+        M.nmaps = m.fmt == KQ_Q6_K ? 0 : Q.nh;
+        if (m.fmt != KQ_Q6_K) {
+            const int box_w = (int)(Q.kb * block_bytes_of(m.fmt) / 8);
+            for (int j = 0; j < Q.nh; ++j) {
+                M.map_h[j] = Q.hs[j];
+                if (!tensor_map(m.W, m.rows, Q.row_bytes, box_w, Q.hs[j], &p.maps[i][j]))
+                    return KQ_ERR_SHAPE;
+            }
+        }
+    }
+    p.nslot = (int)P.nslot;
+    p.slot_bytes = (int)P.slot_bytes;
+    p.x_bytes = 0;
+    p.part_bytes = (int)P.part_bytes;
+    p.scr_bytes = (int)P.scr_bytes;
+    p.ntok = ntok;
+    // always after the fragment pass, which it overlaps
+    p.overlap = 1;
+    for (int hp = 1; hp <= kq::kMaxHinv; ++hp) p.hinv[hp] = ((1u << 20) + hp - 1) / hp;
+    p.hinv[0] = 1u << 20;
+    p.err = info.err;
+    const unsigned long long wl = g_wait_ns.load();
+    p.wait_ns = wl ? wl : kq::kWaitLimitNs;
+    *launched = true;
+    const cudaError_t e = kqlaunch::stream_tc(noct, p, P.grid, (size_t)P.smem, s);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    g_last_kernels = 2 | 4 | 8;
+    g_last_launches = 2;
+    return KQ_OK;
+}
+
 // Kernel choice: the streaming kernel when the shapes can be staged, else
 // the direct-load kernel.  KQ_KERNEL=direct|stream forces one (testing and
 // measurement only; both give bitwise identical results).
@@ -625,6 +868,40 @@ cudaError_t stage_inputs(kq_mat *mats, int n, int ntok, const bool *x_host, cuda
     return cudaSuccess;
 }
 
+// A validated set with ntok >= kq::kTcMinNtok (device pointers): the
+// fragment pass, then one tensor-core launch -- the streaming kernel when
+// it can be staged (unless the direct kernel is selected), else the
+// direct-load kernel.
+kq_status run_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    DeviceInfo info;
+    if (e == cudaSuccess) e = device_info(dev, info);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    const uint8_t *frag[KQ_MAX_SET];
+    const float *aux[KQ_MAX_SET];
+    uint8_t *owned = nullptr;
+    e = prepare_tc_records(mats, n, ntok, s, nullptr, &owned, frag, aux);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    const int choice = kernel_choice();
+    kq_status st = KQ_ERR_SHAPE;
+    bool launched = false;
+    if (choice != 1) st = run_stream_tc(mats, n, ntok, s, info, frag, aux, &launched);
+    if (!launched && choice != 2) st = run_direct_tc(mats, n, ntok, s, info, frag, aux);
+    e = cudaFreeAsync(owned, s);
+    if (st == KQ_OK && e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        st = KQ_ERR_CUDA;
+    }
+    return st;
+}
+
 kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
     const kq_status v = validate_set(in, n, ntok);
     if (v != KQ_OK) return v;
@@ -647,12 +924,18 @@ kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
         return KQ_ERR_CUDA;
     }
     const bool after = staged != nullptr;
-    const int cn = launch_ntok();
-    // near-equal chunks: the first `rem` take one column more
-    const int nch = (ntok + cn - 1) / cn, base = ntok / nch, rem = ntok % nch;
-    kq_mat part[KQ_MAX_SET];
     int kernels = 0, launches = after ? 1 : 0;
     kq_status st = KQ_OK;
+    if (ntok >= kq::kTcMinNtok && tc_enabled()) {
+        st = run_tc(mats, n, ntok, s);
+        kernels = g_last_kernels;
+        launches += g_last_launches;
+    }
+    const int cn = launch_ntok();
+    // dp4a: near-equal chunks, the first `rem` taking one column more
+    const int nch = (ntok >= kq::kTcMinNtok && tc_enabled()) ? 0 : (ntok + cn - 1) / cn;
+    const int base = nch ? ntok / nch : 0, rem = nch ? ntok % nch : 0;
+    kq_mat part[KQ_MAX_SET];
     for (int ci = 0, t0 = 0; ci < nch && st == KQ_OK; ++ci) {
         const int nt = base + (ci < rem ? 1 : 0);
         token_chunk(mats, n, t0, part);
@@ -722,10 +1005,13 @@ kq_status run_noalloc_chunk(const kq_mat &m, int ntok, void *stream);
 kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
     const kq_status v = validate_set(&in, 1, ntok);
     if (v != KQ_OK) return v;
-    // the records of one launch (at most kLaunchNtok tokens) must fit
+    // the records of one launch must fit: the tensor-core fragments of all
+    // ntok columns, or the dp4a records of at most kLaunchNtok columns
     const int nb = (int)(in.cols / 256);
     const bool q6 = in.fmt == KQ_Q6_K;
-    const int64_t rec_total = (int64_t)std::min(ntok, kLaunchNtok) * nb * kq::rec_bytes(q6);
+    const bool tc = ntok >= kq::kTcMinNtok && tc_enabled();
+    const int64_t rec_total = tc ? tc_records_bytes(&in, 1, ntok)
+                                 : (int64_t)std::min(ntok, kLaunchNtok) * nb * kq::rec_bytes(q6);
     if (rec_total > KQ_NOALLOC_RECORD_BYTES) return KQ_ERR_LIMIT;
     int dev = 0;
     const cudaError_t e = cudaGetDevice(&dev);
@@ -738,6 +1024,23 @@ kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
     bool x_host = false;
     const kq_status r = resolve_set(&in, 1, dev, &m, &x_host);
     if (r != KQ_OK) return r;
+    if (tc) {
+        // the fragments into the fixed buffer, then the direct-load kernel
+        DeviceInfo info;
+        uint8_t *buf = nullptr;
+        cudaError_t ce = device_info(dev, info);
+        if (ce == cudaSuccess) ce = noalloc_buffer(dev, &buf);
+        const uint8_t *frag[1];
+        const float *aux[1];
+        uint8_t *owned = nullptr;
+        if (ce == cudaSuccess)
+            ce = prepare_tc_records(&m, 1, ntok, (cudaStream_t)stream, buf, &owned, frag, aux);
+        if (ce != cudaSuccess) {
+            g_last_cuda_error = (int)ce;
+            return KQ_ERR_CUDA;
+        }
+        return run_direct_tc(&m, 1, ntok, (cudaStream_t)stream, info, frag, aux);
+    }
     int launches = 0;
     for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {
         kq_mat part;

@@ -21,7 +21,9 @@ constexpr int kMaxNtok = 8;
 struct MatDesc {
     const uint8_t *W;   // rows * nb super-blocks, row-major
     const float *x;     // [ntok][nb * 256]
-    const uint8_t *rec; // input records [ntok][nb] (kq_xrec.cuh), global memory
+    const uint8_t *rec; // input records [ntok][nb] (kq_xrec.cuh), global memory;
+                        // tensor-core launches: the fragments (kq_xtc.cuh)
+    const float *tc_aux;  // tensor-core launches: the per-token aux array
     float *y;           // [ntok][rows]
     int64_t rows;
     int32_t nb;         // super-blocks per row (cols / 256)
@@ -33,6 +35,8 @@ struct MatDesc {
 struct SetParams {
     MatDesc m[kMaxSet];
     int32_t n;
+    int32_t ntok;  // token columns of the launch (tensor-core launches are
+                   // compiled for a multiple of 8)
 };
 
 // ------------------------------------------------------------ conversions

@@ -16,6 +16,7 @@
 #pragma once
 
 #include "kq_blocks.cuh"
+#include "kq_tc.cuh"
 
 namespace kq {
 
@@ -35,10 +36,67 @@ struct PrepParams {
     int32_t ntok;
 };
 
-template <int NTOK>
+constexpr int kDirectWarps = kDirectThreads / 32;
+
+// Dynamic shared memory of the direct kernel for a member of rpc rows: the
+// partials [nb][rpc][NTOK], then, for tensor-core launches, one unit
+// scratch per warp.
+__host__ __device__ constexpr int64_t direct_part_floats(int nb, int rpc, int ntok) {
+    return ((int64_t)nb * rpc * ntok + 3) / 4 * 4;
+}
+__host__ __device__ constexpr int64_t direct_smem_bytes(int nb, int rpc, int ntok, bool tc) {
+    return 4 * direct_part_floats(nb, rpc, ntok) + (tc ? kDirectWarps * kTcScrBytes : 0);
+}
+
+// The tensor-core form of a CTA: its rows cut into 16-row tiles, each warp
+// taking (tile, block column) units in turn (kq_tc.cuh), weights and input
+// fragments read from global memory.
+template <int NOCT>
+__device__ __forceinline__ void direct_tc(const SetParams &p, const MatDesc &M, int64_t r0,
+                                          int R, float *part_s) {
+    constexpr int NT = 8 * NOCT;
+    const int nb = M.nb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *scr = part_s + direct_part_floats(nb, M.rpc, NT) + warp * (kTcScrBytes / 4);
+    const int bb = M.fmt == kFmtQ4K ? 144 : M.fmt == kFmtQ5K ? 176 : 210;
+    const int64_t rs = (int64_t)nb * bb;
+    const int64_t ostride = (int64_t)nb * kTcFragColBytes, taux = (int64_t)nb * kTcAuxFloats;
+    const int tiles = (R + 15) >> 4;
+#pragma unroll 1
+    for (int u = warp; u < tiles * nb; u += kDirectWarps) {
+        const int b = u / tiles, tile = u - b * tiles;
+        const int rt = tile * 16;
+        const int nvalid = R - rt < 16 ? R - rt : 16;
+        const uint8_t *blk = M.W + (r0 + rt) * rs + (int64_t)b * bb;
+        const uint8_t *frag = M.rec + (int64_t)b * kTcFragColBytes;
+        const float *aux = M.tc_aux + (int64_t)b * kTcAuxFloats;
+        auto rowp = [&](int r) { return blk + r * rs; };
+        float v[NOCT][2][2];
+        if (M.fmt == kFmtQ4K)
+            tc_unit<kFmtQ4K, NOCT, true>(rowp, nvalid, frag, ostride, aux, taux, p.ntok, scr, lane, v);
+        else if (M.fmt == kFmtQ5K)
+            tc_unit<kFmtQ5K, NOCT, true>(rowp, nvalid, frag, ostride, aux, taux, p.ntok, scr, lane, v);
+        else
+            tc_unit<kFmtQ6K, NOCT, true>(rowp, nvalid, frag, ostride, aux, taux, p.ntok, scr, lane, v);
+        const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const int r = rt + g + 8 * k2;
+            if (r < R) {
+#pragma unroll
+                for (int o = 0; o < NOCT; ++o)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        part_s[(b * R + r) * NT + 8 * o + 2 * t4 + j] = v[o][k2][j];
+            }
+        }
+    }
+}
+
+template <int NTOK, bool TC>
 __global__ void __launch_bounds__(kDirectThreads)
     kq_set_direct(const __grid_constant__ SetParams p) {
-    extern __shared__ float part_s[];  // [nb][R][NTOK]
+    extern __shared__ __align__(16) float part_s[];  // [nb][R][NTOK], then scratch
 
     int mi = 0;
 #pragma unroll 1
@@ -48,8 +106,10 @@ __global__ void __launch_bounds__(kDirectThreads)
     const int64_t r0 = (int64_t)((int)blockIdx.x - M.cta_begin) * M.rpc;
     const int R = (int)min((int64_t)M.rpc, M.rows - r0);
     const int nb = M.nb;
+    if constexpr (TC) {
+        direct_tc<NTOK / 8>(p, M, r0, R, part_s);
+    } else {
     const int tasks = R * nb;
-
 #pragma unroll 1
     for (int task = threadIdx.x; task < tasks; task += kDirectThreads) {
         const int b = task / R;
@@ -79,11 +139,13 @@ __global__ void __launch_bounds__(kDirectThreads)
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) part_s[(b * R + r) * NTOK + t] = part[0][t];
     }
+    }
     __syncthreads();
 
 #pragma unroll 1
     for (int o = threadIdx.x; o < R * NTOK; o += kDirectThreads) {
         const int r = o / NTOK, t = o - (o / NTOK) * NTOK;
+        if (TC && t >= p.ntok) continue;
         float s = part_s[r * NTOK + t];
 #pragma unroll 1
         for (int b = 1; b < nb; ++b) s += part_s[(b * R + r) * NTOK + t];

@@ -21,7 +21,8 @@
 // over the consumer warps; each lane turns its two super-blocks into
 // per-token partial sums (kq_blocks.cuh) stored in shared memory.  When a
 // row group's last stage is done, the last warp to finish it sums each
-// row's blocks in block order 0..nb-1 and writes y.  That sum order, and
+// row's blocks in block order 0..nb-1 and writes y; the CTA's last group is
+// summed the same way by all consumer warps together.  That sum order, and
 // each block's arithmetic, depend only on the format, nb and ntok, so a
 // member's output is independent of the grid, the row split and the set.
 //
@@ -34,6 +35,7 @@
 #include <cuda.h>
 
 #include "kq_blocks.cuh"
+#include "kq_tc.cuh"
 
 namespace kq {
 
@@ -48,7 +50,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s (default)
 struct StreamMember {
     const uint8_t *W;
     const float *x;
-    const uint8_t *rec;  // input records in global memory (when not staged)
+    const uint8_t *rec;  // input records in global memory (when not staged);
+                         // tensor-core launches: the fragments (kq_xtc.cuh)
+    const float *tc_aux; // tensor-core launches: the per-token aux array
     float *y;
     int64_t rows;
     int32_t nb;
@@ -74,6 +78,9 @@ struct StreamParams {
     int32_t slot_bytes;
     int32_t x_bytes;     // input records in shared memory (0: in global memory)
     int32_t part_bytes;
+    int32_t scr_bytes;   // tensor-core launches: per-warp unit scratch
+    int32_t ntok;        // token columns of the launch (tensor-core launches
+                         // are compiled for a multiple of 8)
     int32_t overlap;     // launched to overlap the preceding kernel
     uint32_t hinv[kMaxHinv + 1];  // ceil(2^20 / hp): t / hp = (t * hinv[hp]) >> 20
     unsigned int *err;   // device error word (nonzero: a wait expired)
@@ -221,6 +228,9 @@ struct ConsumerCtx {
     const uint8_t *recs;  // this member's input records (shared or global)
     float *part_f;
     int part_floats;      // floats per partial buffer
+    float *scr;           // tensor-core unit scratch (consumer warp 0's; then per warp)
+    const float *tc_aux;
+    int ntok;
     uint32_t bars, ring, xbar;
     int nslot, slot_bytes;
     int nb, kb, nbox, nstage;
@@ -234,6 +244,31 @@ struct ConsumerCtx {
     unsigned int *err;
     unsigned long long wait_ns;
 };
+
+// The CTA's last row group is summed by all consumer warps together once
+// each is done with it (earlier groups are summed by the last warp to
+// finish them, while the others go on): output (token tt, row r) is its nb
+// block partials added in block order, as for every group.  `nt` = token
+// columns of the partial buffer, `ntok` = token columns to store.
+__device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, int ntok,
+                                                  int warp, int lane) {
+    consumer_sync();
+    const int gl = c.G.ng - 1;
+    const int64_t g0 = c.G.start(gl);
+    const int h = (int)(c.G.start(gl + 1) - g0);
+    const float *pbuf = c.part_f + (gl & 1) * c.part_floats;
+    const bool bad = *(volatile int *)c.abort_flag;
+    const int nb = c.nb;
+#pragma unroll 1
+    for (int o = warp * 32 + lane; o < h * ntok; o += kStreamConsumers * 32) {
+        const int tt = o / h, r = o - tt * h;
+        const float *pp = pbuf + (int64_t)r * nb * nt + tt;
+        float acc = pp[0];
+#pragma unroll 4
+        for (int bb = 1; bb < nb; ++bb) acc += pp[bb * nt];
+        c.y[(int64_t)tt * c.rows + g0 + r] = bad ? __int_as_float(0x7FC00000) : acc;
+    }
+}
 
 template <int NTOK, bool XSMEM, int FMT>
 __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane) {
@@ -342,7 +377,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         __syncwarp();
         if (lane == 0) mbar_arrive(c.bars + 8 * (kMaxSlots + slot));
 
-        if (k == c.nbox - 1) {
+        if (k == c.nbox - 1 && g < c.G.ng - 1) {
             // this warp is done with group g
             int old = 0;
             if (lane == 0) {
@@ -385,11 +420,143 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             hinv = c.hinv[hp];
         }
     }
+    reduce_last_group(c, NTOK, NTOK, warp, lane);
 }
 
-template <int NTOK, bool XSMEM>
+// The consumer of a tensor-core launch (ntok >= kTcMinNtok, any format):
+// the stage's work is cut into units of one 16-row tile x one block column
+// (kq_tc.cuh, all NOCT octets of tokens at once), and the CTA's whole
+// sequence of units, stage after stage, is dealt round-robin: warp w takes
+// units w, w + kStreamConsumers, ...  Each warp still waits for every
+// stage's slot and arrives on its empty barrier once per stage (see
+// consume).  The input fragments are read from global memory (L2).
+template <int NOCT, int FMT>
+__device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int lane) {
+    constexpr int NT = 8 * NOCT;
+    constexpr bool Q6 = FMT == kFmtQ6K;
+    constexpr int BB = Q6 ? 210 : (FMT == kFmtQ5K ? 176 : 144);
+    const int nb = c.nb;
+    float *scr = c.scr + warp * (kTcScrBytes / 4);
+    const int64_t ostride = (int64_t)nb * kTcFragColBytes;
+    const int64_t taux = (int64_t)nb * kTcAuxFloats;
+    int next = warp;  // this warp's next unit, counted over the whole CTA
+    int ubase = 0;    // units of the stages before this one
+    int slot = 0, lap = 0, g = 0, k = 0;
+    int64_t g0 = c.G.start(0), g1 = c.G.start(1);
+    int h = (int)(g1 - g0);
+#pragma unroll 1
+    for (int s = 0; s < c.nstage; ++s) {
+        const int b0 = k * c.kb;
+        const int kbv = nb - b0 < c.kb ? nb - b0 : c.kb;
+        const int tiles = (h + 15) >> 4;  // 1 or 2
+        const int units = tiles * kbv;
+        const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
+        float *pbuf = c.part_f + (g & 1) * c.part_floats;
+        bool ok = !*(volatile int *)c.abort_flag;
+        if (ok && k == 0 && g >= 2 &&
+            !mbar_wait(c.xbar + 8 * (g & 1), ((g >> 1) - 1) & 1, c.wait_ns)) {
+            atomicExch(c.abort_flag, 1);
+            atomicOr(c.err, 1u);
+            ok = false;
+        }
+        if (ok && !mbar_wait(c.bars + 8 * slot, lap & 1, c.wait_ns, 128)) {
+            atomicExch(c.abort_flag, 1);
+            atomicOr(c.err, 1u);
+            ok = false;
+        }
+        // Q6_K: a row segment starts as far past a 16-byte boundary as its
+        // first block does in memory (low four bits survive wrap-around)
+        const uint32_t base = (uint32_t)g0 * (uint32_t)c.row_bytes + (uint32_t)b0 * 210u;
+#pragma unroll 1
+        for (; next < ubase + units; next += kStreamConsumers) {
+            if (!ok) continue;
+            const int ul = next - ubase;
+            const int j = tiles == 2 ? ul >> 1 : ul;  // block column within the stage
+            const int r0 = tiles == 2 ? (ul & 1) * 16 : 0;
+            const int nvalid = h - r0 < 16 ? h - r0 : 16;
+            float v[NOCT][2][2];
+            if (!Q6) {
+                const uint8_t *blk = sdp + r0 * (c.kb * BB) + j * BB;
+                const int rs = c.kb * BB;
+                tc_unit<FMT, NOCT, false>([&](int r) { return blk + r * rs; }, nvalid,
+                                          c.recs + (int64_t)(b0 + j) * kTcFragColBytes, ostride,
+                                          c.tc_aux + (int64_t)(b0 + j) * kTcAuxFloats, taux,
+                                          c.ntok, scr, lane, v);
+            } else {
+                const uint32_t rb = (uint32_t)c.row_bytes;
+                tc_unit<FMT, NOCT, false>(
+                    [&](int r) {
+                        const uint32_t m = (base + (uint32_t)(r0 + r) * rb) & 15u;
+                        return sdp + (r0 + r) * c.q6_seg + m + j * 210;
+                    },
+                    nvalid, c.recs + (int64_t)(b0 + j) * kTcFragColBytes, ostride,
+                    c.tc_aux + (int64_t)(b0 + j) * kTcAuxFloats, taux, c.ntok, scr, lane, v);
+            }
+            const int gg = lane >> 2, t4 = lane & 3;
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int row = r0 + gg + 8 * k2;
+                if (row < h) {
+#pragma unroll
+                    for (int o = 0; o < NOCT; ++o)
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj)
+                            pbuf[(row * nb + b0 + j) * NT + 8 * o + 2 * t4 + jj] = v[o][k2][jj];
+                }
+            }
+        }
+        ubase += units;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bars + 8 * (kMaxSlots + slot));
+
+        if (k == c.nbox - 1 && g < c.G.ng - 1) {
+            // this warp is done with group g
+            int old = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                old = atomicAdd(&c.gcount[g & 1], 1);
+            }
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == kStreamConsumers - 1) {
+                __threadfence_block();
+                const bool bad = *(volatile int *)c.abort_flag;
+                if (lane < h) {
+#pragma unroll 1
+                    for (int tt = 0; tt < c.ntok; ++tt) {
+                        float acc = pbuf[(lane * nb) * NT + tt];
+#pragma unroll 4
+                        for (int bb = 1; bb < nb; ++bb) acc += pbuf[(lane * nb + bb) * NT + tt];
+                        c.y[(int64_t)tt * c.rows + g0 + lane] =
+                            bad ? __int_as_float(0x7FC00000) : acc;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    c.gcount[g & 1] = 0;
+                    __threadfence_block();
+                    mbar_arrive(c.xbar + 8 * (g & 1));
+                }
+            }
+        }
+        if (++slot == c.nslot) {
+            slot = 0;
+            ++lap;
+        }
+        if (++k == c.nbox) {
+            k = 0;
+            ++g;
+            g0 = g1;
+            g1 = c.G.start(g + 1);
+            h = (int)(g1 - g0);
+        }
+    }
+    reduce_last_group(c, NT, c.ntok, warp, lane);
+}
+
+template <int NTOK, bool XSMEM, bool TC>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     kq_set_stream(const __grid_constant__ StreamParams p) {
+    static_assert(!TC || (NTOK % 8 == 0 && !XSMEM), "tensor-core launches: octets, global records");
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int abort_flag;
     __shared__ int gcount[2];  // warps done with the row group of each buffer
@@ -415,7 +582,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const uint32_t bars = smem_addr(smem);  // full[0..kMaxSlots), empty[..]
     const uint32_t recs = bars + 1024;
     const uint32_t parts = recs + p.x_bytes;
-    const uint32_t ring = parts + p.part_bytes;
+    const uint32_t scrs = parts + p.part_bytes;
+    const uint32_t ring = scrs + p.scr_bytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t xbar = bars + 8 * (2 * kMaxSlots);  // row group reduced, buffers 0 / 1
@@ -568,6 +736,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.recs_w = smem + (recs - bars);
     c.part_f = reinterpret_cast<float *>(smem + (parts - bars));
     c.part_floats = p.part_bytes / 8;
+    c.scr = reinterpret_cast<float *>(smem + (scrs - bars));
+    c.tc_aux = M.tc_aux;
+    c.ntok = p.ntok;
     c.bars = bars;
     c.ring = ring;
     c.xbar = xbar;
@@ -587,12 +758,21 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.err = p.err;
     c.wait_ns = p.wait_ns;
     c.hinv = p.hinv;
-    if (fmt == kFmtQ4K)
-        consume<NTOK, XSMEM, kFmtQ4K>(c, warp, lane);
-    else if (fmt == kFmtQ5K)
-        consume<NTOK, XSMEM, kFmtQ5K>(c, warp, lane);
-    else
-        consume<NTOK, XSMEM, kFmtQ6K>(c, warp, lane);
+    if constexpr (TC) {
+        if (fmt == kFmtQ4K)
+            consume_tc<NTOK / 8, kFmtQ4K>(c, warp, lane);
+        else if (fmt == kFmtQ5K)
+            consume_tc<NTOK / 8, kFmtQ5K>(c, warp, lane);
+        else
+            consume_tc<NTOK / 8, kFmtQ6K>(c, warp, lane);
+    } else {
+        if (fmt == kFmtQ4K)
+            consume<NTOK, XSMEM, kFmtQ4K>(c, warp, lane);
+        else if (fmt == kFmtQ5K)
+            consume<NTOK, XSMEM, kFmtQ5K>(c, warp, lane);
+        else
+            consume<NTOK, XSMEM, kFmtQ6K>(c, warp, lane);
+    }
 }
 
 }  // namespace kq

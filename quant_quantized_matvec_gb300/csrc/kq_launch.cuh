@@ -15,7 +15,7 @@ namespace kqlaunch {
 
 constexpr int kDirectSmemLimit = 200 * 1024;
 
-template <int NTOK>
+template <int NTOK, bool TC = false>
 cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
                           cudaStream_t stream) {
     static std::mutex mu;
@@ -27,18 +27,18 @@ cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
     if (smem > 48 * 1024) {
         std::lock_guard<std::mutex> lock(mu);
         if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(kq::kq_set_direct<NTOK>,
+            e = cudaFuncSetAttribute(kq::kq_set_direct<NTOK, TC>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kDirectSmemLimit);
             if (e != cudaSuccess) return e;
             configured[dev] = kDirectSmemLimit;
         }
     }
-    kq::kq_set_direct<NTOK><<<grid, kq::kDirectThreads, smem, stream>>>(p);
+    kq::kq_set_direct<NTOK, TC><<<grid, kq::kDirectThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <int NTOK, bool XSMEM>
+template <int NTOK, bool XSMEM, bool TC = false>
 cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cudaStream_t s) {
     static std::mutex mu;
     static size_t configured[64] = {};
@@ -49,7 +49,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
     {
         std::lock_guard<std::mutex> lock(mu);
         if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM>,
+            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM, TC>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             configured[dev] = smem;
@@ -67,7 +67,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM>, p);
+    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM, TC>, p);
 }
 
 // Row gather + dequantization (kq_rows.cu).
@@ -78,23 +78,28 @@ cudaError_t rows(int fmt, const uint8_t *W, int64_t rows, int nb, const int32_t 
 cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
                    cudaStream_t s);
+// tensor-core launches of noct octets of tokens (kq_inst_tc.cu)
+cudaError_t direct_tc(int noct, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t stream_tc(int noct, const kq::StreamParams &p, int grid, size_t smem,
+                      cudaStream_t s);
 
 }  // namespace kqlaunch
 
 #define KQ_DECLARE_INSTANCES(N)                                                            \
     namespace kqlaunch {                                                                   \
-    extern template cudaError_t launch_direct<N>(const kq::SetParams &, int, size_t,       \
-                                                 cudaStream_t);                            \
-    extern template cudaError_t launch_stream<N, true>(const kq::StreamParams &, int,      \
-                                                       size_t, cudaStream_t);              \
-    extern template cudaError_t launch_stream<N, false>(const kq::StreamParams &, int,     \
+    extern template cudaError_t launch_direct<N, false>(const kq::SetParams &, int,        \
                                                         size_t, cudaStream_t);             \
+    extern template cudaError_t launch_stream<N, true, false>(const kq::StreamParams &,    \
+                                                              int, size_t, cudaStream_t);  \
+    extern template cudaError_t launch_stream<N, false, false>(const kq::StreamParams &,   \
+                                                               int, size_t, cudaStream_t); \
     }
 #define KQ_DEFINE_INSTANCES(N)                                                             \
     namespace kqlaunch {                                                                   \
-    template cudaError_t launch_direct<N>(const kq::SetParams &, int, size_t, cudaStream_t); \
-    template cudaError_t launch_stream<N, true>(const kq::StreamParams &, int, size_t,     \
-                                                cudaStream_t);                             \
-    template cudaError_t launch_stream<N, false>(const kq::StreamParams &, int, size_t,    \
+    template cudaError_t launch_direct<N, false>(const kq::SetParams &, int, size_t,       \
                                                  cudaStream_t);                            \
+    template cudaError_t launch_stream<N, true, false>(const kq::StreamParams &, int,      \
+                                                       size_t, cudaStream_t);              \
+    template cudaError_t launch_stream<N, false, false>(const kq::StreamParams &, int,     \
+                                                        size_t, cudaStream_t);             \
     }

@@ -64,7 +64,9 @@ constexpr int kLevels = 5;
 // The geometry of one level (x_bytes: records in shared memory).
 kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int level, Plan &P) {
     const int rcap = kLevelRcap[level], kb_bytes = kLevelKbBytes[level];
-    P.x_bytes = P.part_bytes = P.slot_bytes = P.stages = 0;
+    const bool tc = P.tc_noct > 0;
+    const int ntok_part = tc ? 8 * P.tc_noct : ntok;  // token columns of the partials
+    P.x_bytes = P.part_bytes = P.slot_bytes = P.stages = P.scr_bytes = 0;
     int cta = 0;
     for (int i = 0; i < n; ++i) {
         const kq_mat &m = mats[i];
@@ -79,7 +81,7 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
         M.rows_r = (int)(m.rows % ncta[i]);
         cta += ncta[i];
         // rows per group: partials for the group must fit in 64 KiB
-        const int64_t part_row = (int64_t)nb * ntok * 4;
+        const int64_t part_row = (int64_t)nb * ntok_part * 4;
         const int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
         if (rmax < 1) return KQ_ERR_SHAPE;
         M.rmax = rmax;
@@ -123,9 +125,9 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
                 M.hmax = std::max<int>(M.hmax, (int)hh);
             }
         }
-        // tasks of a stage (row pairs x block columns) stay below 2^12, the
-        // range of the kernel's multiply-shift division
-        {
+        // dp4a launches: tasks of a stage (row pairs x block columns) stay
+        // below 2^12, the range of the kernel's multiply-shift division
+        if (!tc) {
             const int hp = kq::stream_rows_per_task(m.fmt, ntok) == 2 ? (M.hmax + 1) / 2 : M.hmax;
             if ((int64_t)hp * M.kb >= 4096) return KQ_ERR_SHAPE;
         }
@@ -142,24 +144,29 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
         // stages of this member's largest CTA
         P.stages = std::max<int64_t>(P.stages, (int64_t)M.ng[M.rows_r > 0 ? 1 : 0] *
                                                    ((nb + M.kb - 1) / M.kb));
-        // input records [ntok][nb] (kq_xrec.cuh)
-        P.x_bytes = std::max<int64_t>(P.x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
+        // input records [ntok][nb] (kq_xrec.cuh); tensor-core launches read
+        // theirs from global memory
+        if (!tc)
+            P.x_bytes = std::max<int64_t>(P.x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
         P.part_bytes = std::max<int64_t>(P.part_bytes, (int64_t)M.hmax * part_row);
     }
     P.part_bytes = 2 * round_up(P.part_bytes, 128);  // two row groups in flight
     P.slot_bytes = round_up(P.slot_bytes, 128);
     P.x_bytes = round_up(P.x_bytes, 128);
+    if (tc) P.scr_bytes = round_up((int64_t)kq::kStreamConsumers * kq::kTcScrBytes, 128);
     P.grid = cta;
     return KQ_OK;
 }
 
 }  // namespace
 
-kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out) {
+kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out,
+                      int tc_noct) {
     Plan &P = *out;
     P = Plan{};
     P.n = n;
     P.ntok = ntok;
+    P.tc_noct = tc_noct;
     int ncta[KQ_MAX_SET];
     split_ctas(mats, n, sms, ncta);
     // The first level whose input records fit in shared memory beside at
@@ -168,7 +175,7 @@ kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_opt
     // global memory.  The 1 KiB alignment of the dynamic region pads the
     // static part to 1 KiB.
     const int64_t budget = (int64_t)smem_optin - 1024;
-    for (int L = 0; L < kLevels && P.level < 0; ++L) {
+    for (int L = 0; L < kLevels && P.level < 0 && tc_noct == 0; ++L) {
         if (plan_level(mats, n, ntok, ncta, L, P) != KQ_OK) continue;
         const int64_t slots = (budget - 1024 - P.x_bytes - P.part_bytes) / P.slot_bytes;
         const int64_t want = std::min<int64_t>(L == kLevels - 1 ? 2 : 3, std::max<int64_t>(2, P.stages));
@@ -181,7 +188,7 @@ kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_opt
         if (ps != KQ_OK) return ps;
         P.x_bytes = 0;
     }
-    const int64_t fixed = 1024 + P.x_bytes + P.part_bytes;
+    const int64_t fixed = 1024 + P.x_bytes + P.part_bytes + P.scr_bytes;
     P.nslot = std::min<int64_t>(kq::kMaxSlots, (budget - fixed) / P.slot_bytes);
     if (P.nslot < 2) return KQ_ERR_SHAPE;
     P.smem = fixed + P.nslot * P.slot_bytes;
@@ -192,10 +199,13 @@ kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_opt
 
 extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
                                 int64_t *out, int cap) {
-    if (!mats || !out || n < 1 || n > KQ_MAX_SET || ntok < 1 || ntok > 8 || sms < 1) return -1;
+    if (!mats || !out || n < 1 || n > KQ_MAX_SET || ntok < 1 || ntok > KQ_MAX_NTOK || sms < 1)
+        return -1;
     if (cap < KQ_PLAN_HEAD + n * KQ_PLAN_MEMBER) return -1;
     kqplan::Plan P;
-    const kq_status st = kqplan::plan_stream(mats, n, ntok, sms, smem_optin, &P);
+    const int noct = ntok >= kq::kTcMinNtok ? (ntok + 7) / 8 : 0;
+    if (noct == 0 && ntok > 8) return -1;
+    const kq_status st = kqplan::plan_stream(mats, n, ntok, sms, smem_optin, &P, noct);
     int64_t *o = out;
     *o++ = st;
     *o++ = P.grid;
@@ -207,6 +217,7 @@ extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, in
     *o++ = P.nslot;
     *o++ = P.smem;
     *o++ = P.stages;
+    *o++ = P.scr_bytes;
     for (int i = 0; i < n; ++i) {
         const kqplan::Member &M = P.m[i];
         const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],

@@ -1,0 +1,314 @@
+// kq_tc.cuh -- one super-block column of 16 rows against 4..16 token
+// columns on the tensor cores (m16n8k16, f16 operands, f32 accumulation),
+// for Q4_K, Q5_K and Q6_K.
+//
+// Arithmetic ("Chapter 6 - The kquant family on the reference lane",
+// sections 6.2 and 6.4; "Chapter 13 - The QKV + gate matvec family",
+// section 13.4.2 for the deferred scaling).  With the inputs of kq_xtc.cuh
+// (x_j ~ (hi_j + lo_j) * u per token and column) and the codes as f16
+// (the f16 whose bits are an integer k < 2048 has the value k * 2^-24;
+// Q6_K's codes become (q - 32) * 2^-24 by one exact f16 addition), an MMA
+// chain over a sub-block gives
+//
+//   D = 2^-24 * sum_{j in sub-block} c_j * (hi_j + lo_j)
+//
+// for each (row, token), c = q (Q4_K, Q5_K) or q - 32 (Q6_K).  The chain is
+// hi then lo for each k-step of 16 inputs (two k-steps per Q4_K / Q5_K
+// sub-block of 32, one per Q6_K sub-block of 16).  Then, in this fixed
+// order, per row and token of a block:
+//
+//   Q4_K / Q5_K   acc = 0; for s = 0..7:  acc = fma(F_s, D_s, acc),
+//                 F_s = d * sc_s * 2^24 (exact);
+//                 mt  = 0; for s = 0..7:  mt = fma(dm_s, S32_s, mt),
+//                 dm_s = dmin * m_s (exact), S32 the sub-block input sums;
+//                 v   = u * (acc - mt)
+//   Q6_K          acc = 0; for h = 0, 1; kh = 0, 1; q = 0..3, i.e. sub-block
+//                 s = 8h + 2q + kh in that order:  acc = fma(F_s, D_s, acc),
+//                 F_s = d * sc_s * 2^24 (exact);  v = u * acc
+//
+// Every product of a code and an f16 term is exact; the tensor core's sums
+// and these f32 steps round.  A zero Q6_K weight (q = 32) contributes
+// exactly nothing.  A row's v depends only on its bytes and its token's
+// inputs (each MMA output is one row against one token column), never on
+// the tile, the other rows, the other tokens, the kernel or the launch.
+//
+// The k index inside a k-step is permuted (kq_xtc.cuh): lane t of a group
+// of four takes inputs 4t, 4t + 2 (first A register of a row) and 4t + 1,
+// 4t + 3 (second), i.e. bytes 0, 2 and 1, 3 of one 32-bit word of codes.
+#pragma once
+
+#include "kq_common.cuh"
+#include "kq_xtc.cuh"
+
+namespace kq {
+
+// Per-warp scratch of a unit: 16 rows x kTcScrStride floats: F_0..F_15,
+// then (Q4_K / Q5_K) dm_0..dm_7.  112-byte rows: a group of eight rows read
+// together falls on eight different banks.
+constexpr int kTcScrStride = 28;
+constexpr int kTcScrBytes = 16 * kTcScrStride * 4;
+
+// D += A * B over one 16 x 16 x 8 tile, f16 operands, f32 accumulators.
+// (A pure register operation: not volatile, so loads may be scheduled
+// across it.)
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (q - 32) * 2^-24 for both f16 halves of a (codes q * 2^-24, q < 64):
+// exact, the result being a representable f16 (subnormals kept).
+__device__ __forceinline__ uint32_t tc_minus32(uint32_t a) {
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(0x80208020u));
+    return r;
+}
+
+template <bool GLOBAL, class T>
+__device__ __forceinline__ T tc_ld(const void *p) {
+    if (GLOBAL) return __ldg(reinterpret_cast<const T *>(p));
+    return *reinterpret_cast<const T *>(p);
+}
+
+// Float 2^23 + byte k of w (a value below 256).
+__device__ __forceinline__ float tc_magic_byte(uint32_t w, int k) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u | (uint32_t)k));
+}
+
+// A Q6_K block (2-byte aligned): word i (bytes 4i..4i+3) through aligned
+// loads and a funnel shift.  Only a block that starts 2 bytes past a 4-byte
+// boundary reads the aligned word after word i, which lies inside the
+// block for every i < 52.
+template <bool GLOBAL>
+struct Q6Row {
+    const uint8_t *a4;  // block start rounded down to 4 bytes
+    uint32_t sh;        // 16 when the block starts 2 bytes past a 4-byte boundary
+    static __device__ __forceinline__ Q6Row at(const uint8_t *p) {
+        const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(p) & 3u;
+        return {p - mis, mis * 8u};
+    }
+    __device__ __forceinline__ uint32_t word(int i) const {
+        const uint32_t lo = tc_ld<GLOBAL, uint32_t>(a4 + 4 * i);
+        const uint32_t hi = sh ? tc_ld<GLOBAL, uint32_t>(a4 + 4 * i + 4) : 0u;
+        return __funnelshift_r(lo, hi, sh);
+    }
+    __device__ __forceinline__ uint32_t dbits() const {
+        return sh ? (tc_ld<GLOBAL, uint32_t>(a4 + 208) >> 16)
+                  : (uint32_t)tc_ld<GLOBAL, unsigned short>(a4 + 208);
+    }
+};
+
+// The per-row scales of a unit into the warp's scratch: lane = row r (0..15)
+// x half h.  Q4_K / Q5_K: F_s, dm_s for s = 4h..4h+3; Q6_K: F_s for
+// s = 8h..8h+7.  `rowp(r)` is row r's block (rows past nvalid - 1 repeat
+// row nvalid - 1).
+template <int FMT, bool GW, class RowP>
+__device__ __forceinline__ void tc_scales(RowP rowp, int nvalid, float *scr, int lane) {
+    const int r = lane & 15, h = lane >> 4;
+    const uint8_t *p = rowp(r < nvalid ? r : nvalid - 1);
+    float *o = scr + r * kTcScrStride;
+    if (FMT != kFmtQ6K) {
+        const uint4 hd = tc_ld<GW, uint4>(p);
+        const float d24 = h2f(hd.x) * 16777216.0f, nd24 = -d24 * 8388608.0f;
+        const float dmin = h2f(hd.x >> 16), ndm = -dmin * 8388608.0f;
+        const ScaleWords sw = unpack_scale_words(hd.y, hd.z, hd.w);
+        const uint32_t scw = h ? sw.sc_hi : sw.sc_lo, mw = h ? sw.m_hi : sw.m_lo;
+        float4 F, M;
+        F.x = fmaf(d24, tc_magic_byte(scw, 0), nd24);
+        F.y = fmaf(d24, tc_magic_byte(scw, 1), nd24);
+        F.z = fmaf(d24, tc_magic_byte(scw, 2), nd24);
+        F.w = fmaf(d24, tc_magic_byte(scw, 3), nd24);
+        M.x = fmaf(dmin, tc_magic_byte(mw, 0), ndm);
+        M.y = fmaf(dmin, tc_magic_byte(mw, 1), ndm);
+        M.z = fmaf(dmin, tc_magic_byte(mw, 2), ndm);
+        M.w = fmaf(dmin, tc_magic_byte(mw, 3), ndm);
+        *reinterpret_cast<float4 *>(o + 4 * h) = F;
+        *reinterpret_cast<float4 *>(o + 16 + 4 * h) = M;
+    } else {
+        const Q6Row<GW> q = Q6Row<GW>::at(p);
+        const float d24 = h2f(q.dbits()) * 16777216.0f;
+        // signed scale bytes biased to 0..255 for the magic-float decode:
+        // d24 * (F - (2^23 + 128)) with F = 2^23 + (sc + 128)
+        const uint32_t w0 = q.word(48 + 2 * h) ^ 0x80808080u;
+        const uint32_t w1 = q.word(49 + 2 * h) ^ 0x80808080u;
+        float4 F0, F1;
+        F0.x = d24 * (tc_magic_byte(w0, 0) - 8388736.0f);
+        F0.y = d24 * (tc_magic_byte(w0, 1) - 8388736.0f);
+        F0.z = d24 * (tc_magic_byte(w0, 2) - 8388736.0f);
+        F0.w = d24 * (tc_magic_byte(w0, 3) - 8388736.0f);
+        F1.x = d24 * (tc_magic_byte(w1, 0) - 8388736.0f);
+        F1.y = d24 * (tc_magic_byte(w1, 1) - 8388736.0f);
+        F1.z = d24 * (tc_magic_byte(w1, 2) - 8388736.0f);
+        F1.w = d24 * (tc_magic_byte(w1, 3) - 8388736.0f);
+        *reinterpret_cast<float4 *>(o + 8 * h) = F0;
+        *reinterpret_cast<float4 *>(o + 8 * h + 4) = F1;
+    }
+}
+
+// A registers of one k-step from one word of code bytes per row (codes in
+// the bytes' low bits, below 64): rows g (wa) and g + 8 (wb).
+__device__ __forceinline__ void tc_a_from_bytes(uint32_t wa, uint32_t wb, uint32_t mask,
+                                                uint32_t (&a)[4]) {
+    a[0] = wa & mask;         // inputs 4t, 4t + 2 of row g
+    a[1] = wb & mask;         // row g + 8
+    a[2] = (wa >> 8) & mask;  // inputs 4t + 1, 4t + 3 of row g
+    a[3] = (wb >> 8) & mask;
+}
+
+// One unit.  Rows r of the tile at rowp(r) (r < nvalid), one block column,
+// NOCT octets of tokens; `frag` = fragments of (octet 0, this column),
+// `ostride` bytes between octets, `aux` = aux of (token 0, this column),
+// `taux` floats between tokens, `ntok` the launch's token columns.
+// Returns v[o][k2][j] for row g + 8 k2 and token 8o + 2t + j in lane
+// (g, t); tokens past ntok are garbage and not to be stored.
+template <int FMT, int NOCT, bool GW, class RowP>
+__device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *frag,
+                                        int64_t ostride, const float *aux, int64_t taux,
+                                        int ntok, float *scr, int lane,
+                                        float (&v)[NOCT][2][2]) {
+    tc_scales<FMT, GW>(rowp, nvalid, scr, lane);
+    __syncwarp();
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t *pa = rowp(g < nvalid ? g : nvalid - 1);
+    const uint8_t *pb = rowp(g + 8 < nvalid ? g + 8 : nvalid - 1);
+    const float *Fa = scr + g * kTcScrStride, *Fb = scr + (g + 8) * kTcScrStride;
+    float acc[NOCT][2][2];
+#pragma unroll
+    for (int o = 0; o < NOCT; ++o)
+        acc[o][0][0] = acc[o][0][1] = acc[o][1][0] = acc[o][1][1] = 0.0f;
+    const uint8_t *fl = frag + lane * 16;
+    if (FMT != kFmtQ6K) {
+        constexpr bool Q5 = FMT == kFmtQ5K;
+        constexpr int QS = Q5 ? 48 : 16;
+        const uint32_t m4 = 0x000F000Fu, m5 = 0x001F001Fu;
+        uint32_t qha[2] = {0, 0}, qhb[2] = {0, 0};
+        if (Q5) {  // qh bytes 16 * half + 4t .. + 3 of the two rows
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                qha[hf] = tc_ld<GW, uint32_t>(pa + 16 + 16 * hf + 4 * t);
+                qhb[hf] = tc_ld<GW, uint32_t>(pb + 16 + 16 * hf + 4 * t);
+            }
+        }
+#pragma unroll
+        for (int gp = 0; gp < 4; ++gp) {
+            // qs words of k-step halves 0 and 1 of group gp (sub-blocks 2gp, 2gp + 1)
+            uint32_t wa[2], wb[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                wa[hf] = tc_ld<GW, uint32_t>(pa + QS + 32 * gp + 16 * hf + 4 * t);
+                wb[hf] = tc_ld<GW, uint32_t>(pb + QS + 32 * gp + 16 * hf + 4 * t);
+            }
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi) {
+                const int s = 2 * gp + hi;
+                uint32_t A[2][4];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t ca = hi ? (wa[hf] >> 4) & 0x0F0F0F0Fu : wa[hf] & 0x0F0F0F0Fu;
+                    uint32_t cb = hi ? (wb[hf] >> 4) & 0x0F0F0F0Fu : wb[hf] & 0x0F0F0F0Fu;
+                    if (Q5) {  // bit s of each qh byte as bit 4 of the code
+                        ca |= (s <= 4 ? qha[hf] << (4 - s) : qha[hf] >> (s - 4)) & 0x10101010u;
+                        cb |= (s <= 4 ? qhb[hf] << (4 - s) : qhb[hf] >> (s - 4)) & 0x10101010u;
+                    }
+                    tc_a_from_bytes(ca, cb, Q5 ? m5 : m4, A[hf]);
+                }
+                const float fa = Fa[s], fb = Fb[s];
+#pragma unroll
+                for (int o = 0; o < NOCT; ++o) {
+                    const uint8_t *fo = fl + o * ostride;
+                    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const uint4 b = tc_ld<true, uint4>(fo + tc_frag_offset(2 * s + hf, 0));
+                        mma_f16(D, A[hf], b.x, b.y);  // hi
+                        mma_f16(D, A[hf], b.z, b.w);  // lo
+                    }
+                    acc[o][0][0] = fmaf(fa, D[0], acc[o][0][0]);
+                    acc[o][0][1] = fmaf(fa, D[1], acc[o][0][1]);
+                    acc[o][1][0] = fmaf(fb, D[2], acc[o][1][0]);
+                    acc[o][1][1] = fmaf(fb, D[3], acc[o][1][1]);
+                }
+            }
+        }
+        // v = u * (acc - mt), mt = fma chain of dm_s * S32_s over s
+#pragma unroll
+        for (int o = 0; o < NOCT; ++o) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                int tok = 8 * o + 2 * t + j;
+                tok = tok < ntok ? tok : ntok - 1;
+                const float *ax = aux + tok * taux;
+                const float4 s0 = tc_ld<true, float4>(ax + kTcAuxS32);
+                const float4 s1 = tc_ld<true, float4>(ax + kTcAuxS32 + 4);
+                const float u = tc_ld<true, float>(ax + kTcAuxU);
+                const float S[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const float *dm = (k2 ? Fb : Fa) + 16;
+                    float mt = dm[0] * S[0];
+#pragma unroll
+                    for (int s = 1; s < 8; ++s) mt = fmaf(dm[s], S[s], mt);
+                    v[o][k2][j] = u * (acc[o][k2][j] - mt);
+                }
+            }
+        }
+    } else {
+        const Q6Row<GW> qa = Q6Row<GW>::at(pa), qb = Q6Row<GW>::at(pb);
+        const uint32_t m6 = 0x003F003Fu;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int kh = 0; kh < 2; ++kh) {
+                // ql words (quadrant pairs 0/2 and 1/3) and the qh word of
+                // inputs 128h + 16kh + 4t .. (+32q) of the two rows
+                const int w0 = 16 * h + 4 * kh + t, w1 = w0 + 8, wq = 32 + 8 * h + 4 * kh + t;
+                const uint32_t la0 = qa.word(w0), la1 = qa.word(w1), lqa = qa.word(wq);
+                const uint32_t lb0 = qb.word(w0), lb1 = qb.word(w1), lqb = qb.word(wq);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int s = 8 * h + 2 * q + kh;
+                    const uint32_t la = (q & 1) ? la1 : la0, lb = (q & 1) ? lb1 : lb0;
+                    const uint32_t ca = (q < 2 ? la & 0x0F0F0F0Fu : (la >> 4) & 0x0F0F0F0Fu) |
+                                        (((lqa >> (2 * q)) & 0x03030303u) << 4);
+                    const uint32_t cb = (q < 2 ? lb & 0x0F0F0F0Fu : (lb >> 4) & 0x0F0F0F0Fu) |
+                                        (((lqb >> (2 * q)) & 0x03030303u) << 4);
+                    uint32_t A[4];
+                    tc_a_from_bytes(ca, cb, m6, A);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) A[i] = tc_minus32(A[i]);
+                    const float fa = Fa[s], fb = Fb[s];
+#pragma unroll
+                    for (int o = 0; o < NOCT; ++o) {
+                        const uint8_t *fo = fl + o * ostride;
+                        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        const uint4 b = tc_ld<true, uint4>(fo + tc_frag_offset(s, 0));
+                        mma_f16(D, A, b.x, b.y);  // hi
+                        mma_f16(D, A, b.z, b.w);  // lo
+                        acc[o][0][0] = fmaf(fa, D[0], acc[o][0][0]);
+                        acc[o][0][1] = fmaf(fa, D[1], acc[o][0][1]);
+                        acc[o][1][0] = fmaf(fb, D[2], acc[o][1][0]);
+                        acc[o][1][1] = fmaf(fb, D[3], acc[o][1][1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 0; o < NOCT; ++o) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                int tok = 8 * o + 2 * t + j;
+                tok = tok < ntok ? tok : ntok - 1;
+                const float u = tc_ld<true, float>(aux + tok * taux + kTcAuxU);
+                v[o][0][j] = u * acc[o][0][j];
+                v[o][1][j] = u * acc[o][1][j];
+            }
+        }
+    }
+    __syncwarp();  // the scratch is free for the next unit
+}
+
+}  // namespace kq

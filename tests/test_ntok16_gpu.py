@@ -1,7 +1,7 @@
-"""ntok 6..16: the calls that run as several launches of at most 5 token
-columns.  Parity with the oracle, the split's invariant (a token column's
-output is the one a single-column call gives for it, bitwise), the set and
-the no-allocation entry point at these ntok."""
+"""ntok 5..16: the calls that run on the tensor cores, one launch reading W
+once for all their token columns.  Parity with the oracle, the independence
+of the token columns (bitwise, within each of the two arithmetics), the set
+and the no-allocation entry point at these ntok."""
 import ctypes
 
 import numpy as np
@@ -48,8 +48,10 @@ def test_4096x6656_ntok16(fmt):
 @pytest.mark.parametrize("kernel", ["stream", "direct"])
 @pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
 def test_token_columns_are_independent(fmt, kernel):
-    """Output column t of a 16-column call equals, bit for bit, the output
-    of a one-column call on x[t], for both kernels."""
+    """A token column's output does not depend on the other columns: column
+    t of a 16-column call equals, bit for bit, the same column of a
+    5-column call (both on the tensor cores), and column t of a 4-column
+    call equals a one-column call (both dp4a), for both kernels."""
     rows, cols, ntok = 193, 3328, 16
     W, x = C.case(fmt, rows, cols, ntok, f"n16/indep/{fmt}")
     Wd = C.to_dev(W)
@@ -57,17 +59,28 @@ def test_token_columns_are_independent(fmt, kernel):
         kq.select_kernel(kernel)
         g = C.Guarded(ntok, rows)
         kq.matvec(fmt, Wd, rows, cols, C.to_dev(x), y=g.y)
+        quads = []
+        for t0 in (0, 5, 11):
+            q = C.Guarded(5, rows)
+            kq.matvec(fmt, Wd, rows, cols, C.to_dev(x[t0:t0 + 5]), y=q.y)
+            quads.append((t0, q))
+        g3 = C.Guarded(4, rows)
+        kq.matvec(fmt, Wd, rows, cols, C.to_dev(x[2:6]), y=g3.y)
         singles = []
-        for t in (0, 5, 8, 11, 15):
-            s = C.Guarded(1, rows)
-            kq.matvec(fmt, Wd, rows, cols, C.to_dev(x[t:t + 1]), y=s.y)
-            singles.append((t, s))
+        for t in (2, 4):
+            s1 = C.Guarded(1, rows)
+            kq.matvec(fmt, Wd, rows, cols, C.to_dev(x[t:t + 1]), y=s1.y)
+            singles.append((t, s1))
         torch.cuda.synchronize()
     finally:
         kq.select_kernel("auto")
     y = g.host()
-    for t, s in singles:
-        assert np.array_equal(bits(y[t]), bits(s.host()[0])), f"column {t}"
+    for t0, q in quads:
+        assert np.array_equal(bits(y[t0:t0 + 5]), bits(q.host())), f"columns {t0}.."
+    y3 = g3.host()
+    for t, s1 in singles:
+        assert np.array_equal(bits(y3[t - 2]), bits(s1.host()[0])), f"column {t}"
+    C.check(fmt, W, rows, cols, x, y, what=f"{NAMES[fmt]} {kernel} ntok=16")
     assert not kq.device_error()
 
 

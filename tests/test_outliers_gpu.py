@@ -16,6 +16,12 @@ when the outlier sits on a zero weight.  Cases:
   * one input of 1e4 on a zero weight in every row: within the contract;
   * one input of 1e6 on a zero weight in every row: outside the contract,
     as include/kq.h states, but within the contract widened by B.
+Calls of 5 or more token columns run on the tensor cores instead, where
+each input keeps about 22 significant bits and the rounding floor is
+2^(E - 39) for a 256-input column whose largest magnitude is below 2^E
+(kq_xtc.cuh): there every case above, the 1e6 outlier included, is within
+the contract, and a row whose weights are all exactly zero gives exactly
+zero on both paths.
 Both kernels (streaming and direct) are checked against the oracle.
 """
 import numpy as np
@@ -45,10 +51,11 @@ def run(fmt, W, rows, cols, x, kernel):
     return out.host()
 
 
+@pytest.mark.parametrize("ntok", [2, 8])
 @pytest.mark.parametrize("kernel", ["stream", "direct"])
 @pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
-def test_one_outlier_per_group(fmt, kernel):
-    rows, cols, ntok = 300, 2816, 2
+def test_one_outlier_per_group(fmt, kernel, ntok):
+    rows, cols = 300, 2816
     W, x = C.case(fmt, rows, cols, ntok, f"outlier/{fmt}")
     x = x.copy()
     rng = np.random.default_rng(fmt)
@@ -57,19 +64,20 @@ def test_one_outlier_per_group(fmt, kernel):
     for t in range(ntok):
         groups[t, np.arange(groups.shape[1]), pos[t]] *= np.float32(1e3)
     y = run(fmt, W, rows, cols, x, kernel)
-    C.check(fmt, W, rows, cols, x, y, what=f"{NAMES[fmt]} {kernel} outliers")
+    C.check(fmt, W, rows, cols, x, y, what=f"{NAMES[fmt]} {kernel} ntok={ntok} outliers")
 
 
+@pytest.mark.parametrize("ntok", [2, 8])
 @pytest.mark.parametrize("kernel", ["stream", "direct"])
 @pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
-def test_extreme_scales(fmt, kernel):
-    rows, cols, ntok = 77, 1280, 2
+def test_extreme_scales(fmt, kernel, ntok):
+    rows, cols = 77, 1280
     W, x = C.case(fmt, rows, cols, ntok, f"scales/{fmt}")
     x = x.copy()
     x[0] *= np.float32(1e30)
     x[1] *= np.float32(1e-30)
     y = run(fmt, W, rows, cols, x, kernel)
-    C.check(fmt, W, rows, cols, x, y, what=f"{NAMES[fmt]} {kernel} scales")
+    C.check(fmt, W, rows, cols, x, y, what=f"{NAMES[fmt]} {kernel} ntok={ntok} scales")
 
 
 @pytest.mark.parametrize("kernel", ["stream", "direct"])
@@ -91,3 +99,55 @@ def test_outlier_on_a_zero_weight(fmt, kernel):
     err = np.abs(y.astype(np.float64) - y_ref)
     assert np.all(err <= B + tol), (err / (B + tol)).max()
     assert np.any(err_em > tol)  # the case really is outside the contract
+
+
+@pytest.mark.parametrize("kernel", ["stream", "direct"])
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+def test_outlier_on_a_zero_weight_tensor_cores(fmt, kernel):
+    """At ntok = 5 (tensor cores) an input of 1e4 and one of 1e6 on a zero
+    weight both stay within the contract itself."""
+    rows, cols, ntok = 40, 2048, 5
+    W = zero_weight_at_first_input(
+        fmt, C.case(fmt, rows, cols, 1, f"zw/{fmt}")[0].copy())
+    x = C.case(fmt, rows, cols, ntok, f"zw5/{fmt}")[1].copy()
+    for big in (1e4, 1e6):
+        x[:, 0] = np.float32(big)
+        y = run(fmt, W, rows, cols, x, kernel)
+        C.check(fmt, W, rows, cols, x, y,
+                what=f"{NAMES[fmt]} {kernel} ntok={ntok} {big:g} on a zero weight")
+
+
+def zero_rows(fmt, W, idx):
+    """Make every weight of rows `idx` exactly zero (in place), scales left
+    random: Q4_K / Q5_K: all codes 0 and all mins 0 (d*sc*0 - dmin*0);
+    Q6_K: all codes 32 (d*sc*(32 - 32))."""
+    bb = C.synth.BLOCK_BYTES[fmt]
+    blocks = W.reshape(W.shape[0], -1, bb)
+    assert np.shares_memory(blocks, W)
+    if fmt == kq.Q6_K:
+        blocks[idx, :, 0:128] = 0          # ql: code bits 0..3
+        blocks[idx, :, 128:192] = 0xAA     # qh: code bits 4..5 = 0b10
+    else:
+        blocks[idx, :, 8:12] = 0           # scales[4..7]: m_0..3, top bits of m_4..7
+        blocks[idx, :, 12:16] &= 0x0F      # scales[8..11]: low bits of m_4..7
+        qs = 48 if fmt == kq.Q5_K else 16
+        blocks[idx, :, qs:qs + 128] = 0    # code low bits
+        if fmt == kq.Q5_K:
+            blocks[idx, :, 16:48] = 0      # qh: code bit 4
+    return W
+
+
+@pytest.mark.parametrize("ntok", [1, 3, 8])
+@pytest.mark.parametrize("kernel", ["stream", "direct"])
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+def test_zero_weight_rows_give_zero(fmt, kernel, ntok):
+    """Rows whose weights are all exactly zero give exactly zero (S = 0, so
+    the contract allows only the absolute 1e-6), on the dp4a and the
+    tensor-core arithmetic, with ordinary rows around them."""
+    rows, cols = 96, 2560
+    W, x = C.case(fmt, rows, cols, ntok, f"zrow/{fmt}/{ntok}")
+    W = np.ascontiguousarray(W).copy()
+    zero_rows(fmt, W, np.arange(0, rows, 3))
+    y = run(fmt, W, rows, cols, x, kernel)
+    assert np.all(y[:, ::3] == 0.0), np.abs(y[:, ::3]).max()
+    C.check(fmt, W, rows, cols, x, y, what=f"{NAMES[fmt]} {kernel} ntok={ntok} zero rows")

@@ -5,8 +5,9 @@ an allocator or a memory budget that forbids hidden allocations, and loops
 that must not take an allocator's locks.  kq_matvec_noalloc serves them with
 the direct-load kernel and one fixed device buffer for its input records.
 Its results must be bitwise those of kq_matvec with the direct-load kernel
-selected, on two calls in a row that reuse the buffer, on a call that runs
-as two launches in turn on the buffer (ntok = 12), and with x in pinned host
+selected, on two calls in a row that reuse the buffer, on calls of the
+tensor-core path (ntok = 5 and 12, whose input fragments take the buffer),
+and with x in pinned host
 memory (read in place, since staging would allocate); each is also checked
 against the oracle.  Calls beyond the buffer are refused.
 
@@ -71,8 +72,8 @@ def test_noalloc_calls_in_a_row_bitwise_equal_direct_kq_matvec():
         for fmt, rows, cols, ntok, W, x, Wd, xd in inputs:
             g = C.Guarded(ntok, rows)
             assert _call(lib.kq_matvec_noalloc, fmt, Wd, rows, cols, xd, g.y, ntok) == KQ_OK
-            # ntok = 12 runs as two launches of the record pass and the kernel
-            assert lib.kq_last_launch_count() == (4 if ntok > 8 else 2)
+            # the record (or fragment) pass and the kernel
+            assert lib.kq_last_launch_count() == 2
             outs.append(g)
         torch.cuda.synchronize()
         for (fmt, rows, cols, ntok, W, x, Wd, xd), g in zip(inputs, outs):
@@ -102,9 +103,10 @@ def test_noalloc_reads_pinned_host_x_in_place():
 def test_noalloc_rejects_records_beyond_its_buffer():
     lib = _binding.load()
     ntok, fmt = 8, kq.Q6_K
-    # ntok * (cols / 256) * 1056 > 1 MiB  ->  cols = 256 * 125
+    # tensor-core fragments of one octet, 8192 bytes per 256 inputs, plus
+    # 64 bytes per token and 256 inputs, above 1 MiB  ->  cols = 256 * 125
     cols = 256 * 125
-    assert ntok * (cols // 256) * 1056 > NOALLOC_RECORD_BYTES
+    assert (cols // 256) * (8192 + ntok * 64) > NOALLOC_RECORD_BYTES
     rows = 2
     W, x = C.case(fmt, rows, cols, ntok, "noalloc/limit")
     Wd, xd = C.to_dev(W), C.to_dev(x)
