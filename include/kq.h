@@ -242,11 +242,12 @@ kq_status kq_device_error(int clear);
  * Kernel selection, for testing and measurement: 0 = automatic (the
  * TMA-streaming kernel whenever the shapes can be staged in shared memory,
  * else the direct-load kernel), 1 = always the direct-load kernel, 2 = only
- * the streaming kernel (calls it cannot stage return KQ_ERR_SHAPE).  Both
- * kernels compute every output with the same arithmetic in the same order,
- * so results do not depend on this setting.  Process-wide; the environment
- * variable KQ_KERNEL=direct|stream sets the initial value.  Returns the
- * previous setting; an argument outside 0..2 only queries.
+ * the streaming kernel (calls it cannot stage return KQ_ERR_SHAPE with
+ * nothing enqueued).  Both kernels compute every output with the same
+ * arithmetic in the same order, so results do not depend on this setting.
+ * Process-wide; the environment variable KQ_KERNEL=direct|stream sets the
+ * initial value.  Returns the previous setting; an argument outside 0..2
+ * only queries.
  */
 int kq_select_kernel(int which);
 

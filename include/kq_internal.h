@@ -15,12 +15,12 @@ extern "C" {
 
 /* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
  * KQ_PLAN_MEMBER per member. */
-#define KQ_PLAN_HEAD 11
+#define KQ_PLAN_HEAD 12
 #define KQ_PLAN_MEMBER 20
 
 /*
  * The streaming kernel's launch geometry for the set `mats` (n members,
- * ntok token columns in the launch: 1..3 for the dp4a kernels, 4..16 for
+ * ntok token columns in the launch: 1..4 for the dp4a kernels, 5..16 for
  * the tensor-core kernels, as the library chooses) on a device with `sms` SMs and
  * `smem_optin` bytes of opt-in shared memory per CTA, as the library would
  * plan it.  Pure host arithmetic on the descriptors' shapes and formats
@@ -32,6 +32,8 @@ extern "C" {
  *   shared memory (0/1)  [4] x_bytes  [5] part_bytes  [6] slot_bytes
  *   [7] nslot  [8] dynamic shared memory  [9] stages of the largest CTA
  *   [10] bytes of the tensor-core units' scratch (0 for dp4a launches)
+ *   [11] partial buffers (2; 1 for a tensor-core launch whose CTAs have
+ *   one row group each)
  *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
  *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes.
  * Returns 0, or -1 for bad arguments (nothing written).

@@ -111,8 +111,7 @@ __global__ void __launch_bounds__(kStageThreads) kq_xstage(const __grid_constant
 // set.
 struct TcPrepParams {
     const float *x[KQ_MAX_SET];
-    uint8_t *frag[KQ_MAX_SET];
-    float *aux[KQ_MAX_SET];
+    uint8_t *rec[KQ_MAX_SET];
     int32_t nb[KQ_MAX_SET];
     int64_t first_warp[KQ_MAX_SET + 1];
     int32_t n, ntok;
@@ -134,11 +133,12 @@ __global__ void __launch_bounds__(kTcPrepThreads) kq_xprep_tc(const __grid_const
         if (w >= p.first_warp[i]) k = i;
     const int i = (int)(w - p.first_warp[k]);
     const int nb = p.nb[k];
+    const int noct = (p.ntok + 7) / 8;
     const int q = i % kTcPrepSplit, oj = i / kTcPrepSplit;
     const int o = oj / nb, j = oj - o * nb;
-    build_tc_record(p.x[k], p.ntok, nb, o, j, q,
-                    p.frag[k] + ((int64_t)o * nb + j) * kTcFragColBytes, p.aux[k],
-                    threadIdx.x & 31);
+    uint8_t *col = p.rec[k] + (int64_t)j * tc_col_bytes(noct);
+    build_tc_record(p.x[k], p.ntok, nb, o, j, q, col + o * kTcFragOctBytes,
+                    reinterpret_cast<float *>(col + noct * kTcFragOctBytes), threadIdx.x & 31);
 }
 
 }  // namespace kq
@@ -530,6 +530,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.slot_bytes = (int)P.slot_bytes;
     p.x_bytes = (int)P.x_bytes;
     p.part_bytes = (int)P.part_bytes;
+    p.part_bufs = P.part_bufs;
     // Launch overlap: as set by kq_set_overlap, and always right after the
     // staging kernel, which writes nothing this launch reads before its
     // griddepcontrol.wait.
@@ -580,9 +581,9 @@ int tc_enabled() {
     return c;
 }
 
-// Fragments of every member in `buf` (caller-provided, or a stream-ordered
-// temporary when buf is null: *owned is then set).  frag[i] / aux[i]:
-// member i's fragments and aux array.
+// Tensor-core records (kq_xtc.cuh) of every member in `buf` (caller-
+// provided, or a stream-ordered temporary when buf is null: *owned is then
+// set), one per distinct input plane; rec[i]: member i's records.
 int64_t tc_records_bytes(const kq_mat *mats, int n, int ntok) {
     int64_t total = 0;
     for (int i = 0; i < n; ++i) {
@@ -595,7 +596,7 @@ int64_t tc_records_bytes(const kq_mat *mats, int n, int ntok) {
 }
 
 cudaError_t prepare_tc_records(const kq_mat *mats, int n, int ntok, cudaStream_t s, uint8_t *buf,
-                               uint8_t **owned, const uint8_t **frag, const float **aux) {
+                               uint8_t **owned, const uint8_t **rec) {
     *owned = nullptr;
     const int64_t total = tc_records_bytes(mats, n, ntok);
     if (!buf) {
@@ -617,15 +618,13 @@ cudaError_t prepare_tc_records(const kq_mat *mats, int n, int ntok, cudaStream_t
             const int nb = (int)(mats[i].cols / 256);
             p.x[k] = mats[i].x;
             p.nb[k] = nb;
-            p.frag[k] = buf + off;
-            p.aux[k] = reinterpret_cast<float *>(buf + off + kq::tc_frag_bytes(noct, nb));
+            p.rec[k] = buf + off;
             off += (kq::tc_record_bytes(ntok, nb) + 255) / 256 * 256;
             p.first_warp[k] = warps;
             warps += (int64_t)noct * nb * kq::kTcPrepSplit;
             plane_of[i] = k;
         }
-        frag[i] = p.frag[plane_of[i]];
-        aux[i] = p.aux[plane_of[i]];
+        rec[i] = p.rec[plane_of[i]];
     }
     p.first_warp[p.n] = warps;
     const int64_t blocks = (warps * 32 + kq::kTcPrepThreads - 1) / kq::kTcPrepThreads;
@@ -663,8 +662,7 @@ int64_t direct_tc_rows_per_cta(const kq_mat &m, int ntok, int sms) {
 }
 
 kq_status run_direct_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
-                        const DeviceInfo &info, const uint8_t *const *frag,
-                        const float *const *aux) {
+                        const DeviceInfo &info, const uint8_t *const *rec) {
     kq::SetParams p{};
     p.n = n;
     p.ntok = ntok;
@@ -678,8 +676,7 @@ kq_status run_direct_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         if (rpc < 1) return KQ_ERR_SHAPE;
         p.m[i].W = (const uint8_t *)m.W;
         p.m[i].x = m.x;
-        p.m[i].rec = frag[i];
-        p.m[i].tc_aux = aux[i];
+        p.m[i].rec = rec[i];
         p.m[i].y = m.y;
         p.m[i].rows = m.rows;
         p.m[i].nb = nb;
@@ -701,8 +698,7 @@ kq_status run_direct_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
 }
 
 kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
-                        const DeviceInfo &info, const uint8_t *const *frag,
-                        const float *const *aux, bool *launched) {
+                        const DeviceInfo &info, const uint8_t *const *rec, bool *launched) {
     *launched = false;
     static kq::StreamParams p;  // ~10 KB: kept off the stack
     static std::mutex pmu;
@@ -719,8 +715,7 @@ kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         kq::StreamMember &M = p.m[i];
         M.W = (const uint8_t *)m.W;
         M.x = m.x;
-        M.rec = frag[i];
-        M.tc_aux = aux[i];
+        M.rec = rec[i];
         M.y = m.y;
         M.rows = m.rows;
         M.nb = (int)(m.cols / 256);
@@ -751,6 +746,7 @@ kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     p.slot_bytes = (int)P.slot_bytes;
     p.x_bytes = 0;
     p.part_bytes = (int)P.part_bytes;
+    p.part_bufs = P.part_bufs;
     p.scr_bytes = (int)P.scr_bytes;
     p.ntok = ntok;
     // always after the fragment pass, which it overlaps
@@ -881,19 +877,26 @@ kq_status run_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
     }
-    const uint8_t *frag[KQ_MAX_SET];
-    const float *aux[KQ_MAX_SET];
+    // the streaming kernel, when forced but unable to take the call, fails
+    // before anything is enqueued
+    const int choice = kernel_choice();
+    if (choice == 2) {
+        kqplan::Plan PS;
+        const kq_status ps =
+            kqplan::plan_stream(mats, n, ntok, info.sms, info.smem_optin, &PS, (ntok + 7) / 8);
+        if (ps != KQ_OK) return ps;
+    }
+    const uint8_t *rec[KQ_MAX_SET];
     uint8_t *owned = nullptr;
-    e = prepare_tc_records(mats, n, ntok, s, nullptr, &owned, frag, aux);
+    e = prepare_tc_records(mats, n, ntok, s, nullptr, &owned, rec);
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
     }
-    const int choice = kernel_choice();
     kq_status st = KQ_ERR_SHAPE;
     bool launched = false;
-    if (choice != 1) st = run_stream_tc(mats, n, ntok, s, info, frag, aux, &launched);
-    if (!launched && choice != 2) st = run_direct_tc(mats, n, ntok, s, info, frag, aux);
+    if (choice != 1) st = run_stream_tc(mats, n, ntok, s, info, rec, &launched);
+    if (!launched && choice != 2) st = run_direct_tc(mats, n, ntok, s, info, rec);
     e = cudaFreeAsync(owned, s);
     if (st == KQ_OK && e != cudaSuccess) {
         g_last_cuda_error = (int)e;
@@ -1030,16 +1033,15 @@ kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
         uint8_t *buf = nullptr;
         cudaError_t ce = device_info(dev, info);
         if (ce == cudaSuccess) ce = noalloc_buffer(dev, &buf);
-        const uint8_t *frag[1];
-        const float *aux[1];
+        const uint8_t *rec[1];
         uint8_t *owned = nullptr;
         if (ce == cudaSuccess)
-            ce = prepare_tc_records(&m, 1, ntok, (cudaStream_t)stream, buf, &owned, frag, aux);
+            ce = prepare_tc_records(&m, 1, ntok, (cudaStream_t)stream, buf, &owned, rec);
         if (ce != cudaSuccess) {
             g_last_cuda_error = (int)ce;
             return KQ_ERR_CUDA;
         }
-        return run_direct_tc(&m, 1, ntok, (cudaStream_t)stream, info, frag, aux);
+        return run_direct_tc(&m, 1, ntok, (cudaStream_t)stream, info, rec);
     }
     int launches = 0;
     for (int t0 = 0; t0 < ntok; t0 += kLaunchNtok) {

@@ -22,8 +22,7 @@ struct MatDesc {
     const uint8_t *W;   // rows * nb super-blocks, row-major
     const float *x;     // [ntok][nb * 256]
     const uint8_t *rec; // input records [ntok][nb] (kq_xrec.cuh), global memory;
-                        // tensor-core launches: the fragments (kq_xtc.cuh)
-    const float *tc_aux;  // tensor-core launches: the per-token aux array
+                        // tensor-core launches: the records of kq_xtc.cuh
     float *y;           // [ntok][rows]
     int64_t rows;
     int32_t nb;         // super-blocks per row (cols / 256)

@@ -60,7 +60,7 @@ __device__ __forceinline__ void direct_tc(const SetParams &p, const MatDesc &M, 
     float *scr = part_s + direct_part_floats(nb, M.rpc, NT) + warp * (kTcScrBytes / 4);
     const int bb = M.fmt == kFmtQ4K ? 144 : M.fmt == kFmtQ5K ? 176 : 210;
     const int64_t rs = (int64_t)nb * bb;
-    const int64_t ostride = (int64_t)nb * kTcFragColBytes, taux = (int64_t)nb * kTcAuxFloats;
+    constexpr int colb = tc_col_bytes(NOCT);
     const int tiles = (R + 15) >> 4;
 #pragma unroll 1
     for (int u = warp; u < tiles * nb; u += kDirectWarps) {
@@ -68,16 +68,15 @@ __device__ __forceinline__ void direct_tc(const SetParams &p, const MatDesc &M, 
         const int rt = tile * 16;
         const int nvalid = R - rt < 16 ? R - rt : 16;
         const uint8_t *blk = M.W + (r0 + rt) * rs + (int64_t)b * bb;
-        const uint8_t *frag = M.rec + (int64_t)b * kTcFragColBytes;
-        const float *aux = M.tc_aux + (int64_t)b * kTcAuxFloats;
+        const uint8_t *col = M.rec + (int64_t)b * colb;  // this column's records
         auto rowp = [&](int r) { return blk + r * rs; };
         float v[NOCT][2][2];
         if (M.fmt == kFmtQ4K)
-            tc_unit<kFmtQ4K, NOCT, true>(rowp, nvalid, frag, ostride, aux, taux, p.ntok, scr, lane, v);
+            tc_unit<kFmtQ4K, NOCT, true, true>(rowp, nvalid, col, p.ntok, scr, lane, v);
         else if (M.fmt == kFmtQ5K)
-            tc_unit<kFmtQ5K, NOCT, true>(rowp, nvalid, frag, ostride, aux, taux, p.ntok, scr, lane, v);
+            tc_unit<kFmtQ5K, NOCT, true, true>(rowp, nvalid, col, p.ntok, scr, lane, v);
         else
-            tc_unit<kFmtQ6K, NOCT, true>(rowp, nvalid, frag, ostride, aux, taux, p.ntok, scr, lane, v);
+            tc_unit<kFmtQ6K, NOCT, true, true>(rowp, nvalid, col, p.ntok, scr, lane, v);
         const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {

@@ -51,8 +51,7 @@ struct StreamMember {
     const uint8_t *W;
     const float *x;
     const uint8_t *rec;  // input records in global memory (when not staged);
-                         // tensor-core launches: the fragments (kq_xtc.cuh)
-    const float *tc_aux; // tensor-core launches: the per-token aux array
+                         // tensor-core launches: the records of kq_xtc.cuh
     float *y;
     int64_t rows;
     int32_t nb;
@@ -78,6 +77,7 @@ struct StreamParams {
     int32_t slot_bytes;
     int32_t x_bytes;     // input records in shared memory (0: in global memory)
     int32_t part_bytes;
+    int32_t part_bufs;   // partial buffers: 2, or 1 when no CTA has a second row group
     int32_t scr_bytes;   // tensor-core launches: per-warp unit scratch
     int32_t ntok;        // token columns of the launch (tensor-core launches
                          // are compiled for a multiple of 8)
@@ -227,9 +227,8 @@ struct ConsumerCtx {
     int *xissued;         // consumer warps whose input loads have gone out
     const uint8_t *recs;  // this member's input records (shared or global)
     float *part_f;
-    int part_floats;      // floats per partial buffer
+    int part_step;        // floats from partial buffer 0 to 1 (0: one buffer)
     float *scr;           // tensor-core unit scratch (consumer warp 0's; then per warp)
-    const float *tc_aux;
     int ntok;
     uint32_t bars, ring, xbar;
     int nslot, slot_bytes;
@@ -256,7 +255,7 @@ __device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, 
     const int gl = c.G.ng - 1;
     const int64_t g0 = c.G.start(gl);
     const int h = (int)(c.G.start(gl + 1) - g0);
-    const float *pbuf = c.part_f + (gl & 1) * c.part_floats;
+    const float *pbuf = c.part_f + (gl & 1) * c.part_step;
     const bool bad = *(volatile int *)c.abort_flag;
     const int nb = c.nb;
 #pragma unroll 1
@@ -303,7 +302,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         const int tasks = hp * kbv;
         const int nbat = (int)(((uint32_t)tasks + 31u) >> 5);
         const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
-        float *pbuf = c.part_f + (g & 1) * c.part_floats;
+        float *pbuf = c.part_f + (g & 1) * c.part_step;
         bool ok = !*(volatile int *)c.abort_flag;
         if (ok && k == 0 && g >= 2 &&
             !mbar_wait(c.xbar + 8 * (g & 1), ((g >> 1) - 1) & 1, c.wait_ns)) {
@@ -429,7 +428,8 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
 // sequence of units, stage after stage, is dealt round-robin: warp w takes
 // units w, w + kStreamConsumers, ...  Each warp still waits for every
 // stage's slot and arrives on its empty barrier once per stage (see
-// consume).  The input fragments are read from global memory (L2).
+// consume).  The input records (kq_xtc.cuh) are read from global memory
+// (L2, then L1).
 template <int NOCT, int FMT>
 __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int lane) {
     constexpr int NT = 8 * NOCT;
@@ -437,8 +437,7 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
     constexpr int BB = Q6 ? 210 : (FMT == kFmtQ5K ? 176 : 144);
     const int nb = c.nb;
     float *scr = c.scr + warp * (kTcScrBytes / 4);
-    const int64_t ostride = (int64_t)nb * kTcFragColBytes;
-    const int64_t taux = (int64_t)nb * kTcAuxFloats;
+    constexpr int colb = tc_col_bytes(NOCT);
     int next = warp;  // this warp's next unit, counted over the whole CTA
     int ubase = 0;    // units of the stages before this one
     int slot = 0, lap = 0, g = 0, k = 0;
@@ -451,7 +450,7 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
         const int tiles = (h + 15) >> 4;  // 1 or 2
         const int units = tiles * kbv;
         const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
-        float *pbuf = c.part_f + (g & 1) * c.part_floats;
+        float *pbuf = c.part_f + (g & 1) * c.part_step;
         bool ok = !*(volatile int *)c.abort_flag;
         if (ok && k == 0 && g >= 2 &&
             !mbar_wait(c.xbar + 8 * (g & 1), ((g >> 1) - 1) & 1, c.wait_ns)) {
@@ -475,22 +474,20 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
             const int r0 = tiles == 2 ? (ul & 1) * 16 : 0;
             const int nvalid = h - r0 < 16 ? h - r0 : 16;
             float v[NOCT][2][2];
+            const uint8_t *col = c.recs + (int64_t)(b0 + j) * colb;  // column b0 + j's records
             if (!Q6) {
                 const uint8_t *blk = sdp + r0 * (c.kb * BB) + j * BB;
                 const int rs = c.kb * BB;
-                tc_unit<FMT, NOCT, false>([&](int r) { return blk + r * rs; }, nvalid,
-                                          c.recs + (int64_t)(b0 + j) * kTcFragColBytes, ostride,
-                                          c.tc_aux + (int64_t)(b0 + j) * kTcAuxFloats, taux,
-                                          c.ntok, scr, lane, v);
+                tc_unit<FMT, NOCT, false, true>([&](int r) { return blk + r * rs; }, nvalid, col,
+                                                c.ntok, scr, lane, v);
             } else {
                 const uint32_t rb = (uint32_t)c.row_bytes;
-                tc_unit<FMT, NOCT, false>(
+                tc_unit<FMT, NOCT, false, true>(
                     [&](int r) {
                         const uint32_t m = (base + (uint32_t)(r0 + r) * rb) & 15u;
                         return sdp + (r0 + r) * c.q6_seg + m + j * 210;
                     },
-                    nvalid, c.recs + (int64_t)(b0 + j) * kTcFragColBytes, ostride,
-                    c.tc_aux + (int64_t)(b0 + j) * kTcAuxFloats, taux, c.ntok, scr, lane, v);
+                    nvalid, col, c.ntok, scr, lane, v);
             }
             const int gg = lane >> 2, t4 = lane & 3;
 #pragma unroll
@@ -735,9 +732,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.recs = XSMEM ? smem + (recs - bars) : M.rec;
     c.recs_w = smem + (recs - bars);
     c.part_f = reinterpret_cast<float *>(smem + (parts - bars));
-    c.part_floats = p.part_bytes / 8;
+    c.part_step = p.part_bufs == 2 ? p.part_bytes / 8 : 0;
     c.scr = reinterpret_cast<float *>(smem + (scrs - bars));
-    c.tc_aux = M.tc_aux;
     c.ntok = p.ntok;
     c.bars = bars;
     c.ring = ring;

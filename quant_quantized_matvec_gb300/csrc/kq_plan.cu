@@ -55,6 +55,21 @@ void split_ctas(const kq_mat *mats, int n, int G, int *ncta) {
     }
 }
 
+// Q6_K: bytes between row segments in a slot.  A segment of kb blocks
+// starts up to 14 bytes past a 16-byte boundary and its copy ends up to 14
+// bytes past its end; an odd number of 16-byte units puts consecutive rows
+// on different banks.
+int q6_seg(int kb) {
+    int seg = (int)round_up((int64_t)kb * 210 + 28, 16);
+    if (((seg / 16) & 1) == 0) seg += 16;
+    return seg;
+}
+
+// Weight bytes of a stage slot: h rows of kb blocks.
+int64_t stage_weight_bytes(int fmt, int h, int kb) {
+    return fmt == KQ_Q6_K ? (int64_t)h * q6_seg(kb) : (int64_t)h * kb * block_bytes(fmt);
+}
+
 // Stage geometry levels, from the largest stages down: stages are
 // [h rows][kb blocks] with h <= rcap and stage rows of at most kb_bytes.
 constexpr int kLevelRcap[] = {32, 16, 16, 8, 8};
@@ -67,6 +82,7 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
     const bool tc = P.tc_noct > 0;
     const int ntok_part = tc ? 8 * P.tc_noct : ntok;  // token columns of the partials
     P.x_bytes = P.part_bytes = P.slot_bytes = P.stages = P.scr_bytes = 0;
+    P.part_bufs = 1;
     int cta = 0;
     for (int i = 0; i < n; ++i) {
         const kq_mat &m = mats[i];
@@ -92,24 +108,6 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
             M.gq[big] = (int)(nn / ng);
             M.gr[big] = (int)(nn % ng);
         }
-        // Blocks per stage row: at most kb_bytes (and 256 u64); prefer few
-        // stages per row, then no zero-filled tail, then an odd number of
-        // 16-byte units per row (rows on distinct banks).
-        {
-            const int kbmax = (int)std::max<int64_t>(1, std::min<int64_t>(nb, kb_bytes / bb));
-            int best = 1;
-            int64_t best_key = INT64_MAX;
-            for (int kb = 1; kb <= kbmax; ++kb) {
-                const int64_t nbox = (nb + kb - 1) / kb, waste = nbox * kb - nb;
-                const int64_t units = (int64_t)kb * bb / 16;
-                const int64_t key = nbox * 1000000 + waste * 10 + ((units & 1) ? 0 : 1);
-                if (key < best_key) {
-                    best_key = key;
-                    best = kb;
-                }
-            }
-            M.kb = best;
-        }
         // group heights that occur: n in {floor, ceil}(rows / ncta)
         const int64_t nlo = m.rows / ncta[i], nhi = (m.rows + ncta[i] - 1) / ncta[i];
         for (int64_t nn = nlo; nn <= nhi; ++nn) {
@@ -125,22 +123,35 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
                 M.hmax = std::max<int>(M.hmax, (int)hh);
             }
         }
+        // Blocks per stage row: at most kb_bytes (and 256 u64); prefer few
+        // stages per row, then no zero-filled tail, then an odd number of
+        // 16-byte units per row (rows on distinct banks).
+        {
+            const int kbmax = (int)std::max<int64_t>(1, std::min<int64_t>(nb, kb_bytes / bb));
+            int best = 0;
+            int64_t best_key = INT64_MAX;
+            for (int kb = 1; kb <= kbmax; ++kb) {
+                const int64_t nbox = (nb + kb - 1) / kb, waste = nbox * kb - nb;
+                const int64_t units = (int64_t)kb * bb / 16;
+                const int64_t key = nbox * 1000000 + waste * 10 + ((units & 1) ? 0 : 1);
+                if (key < best_key) {
+                    best_key = key;
+                    best = kb;
+                }
+            }
+            if (best == 0) return KQ_ERR_SHAPE;
+            M.kb = best;
+        }
         // dp4a launches: tasks of a stage (row pairs x block columns) stay
         // below 2^12, the range of the kernel's multiply-shift division
         if (!tc) {
             const int hp = kq::stream_rows_per_task(m.fmt, ntok) == 2 ? (M.hmax + 1) / 2 : M.hmax;
             if ((int64_t)hp * M.kb >= 4096) return KQ_ERR_SHAPE;
         }
-        if (m.fmt != KQ_Q6_K) {
-            P.slot_bytes = std::max<int64_t>(P.slot_bytes, (int64_t)M.hmax * M.kb * bb);
-        } else {
-            // a segment of kb blocks starts up to 14 bytes past a 16-byte
-            // boundary and its copy ends up to 14 bytes past its end
-            int seg = (int)round_up((int64_t)M.kb * 210 + 28, 16);
-            if (((seg / 16) & 1) == 0) seg += 16;
-            M.seg = seg;
-            P.slot_bytes = std::max<int64_t>(P.slot_bytes, (int64_t)M.hmax * seg);
-        }
+        if (m.fmt == KQ_Q6_K) M.seg = q6_seg(M.kb);
+        P.slot_bytes = std::max<int64_t>(P.slot_bytes, stage_weight_bytes(m.fmt, M.hmax, M.kb));
+        // CTAs of rows_q (+ 1) rows exist when rows_r < ncta (rows_r > 0)
+        if ((M.rows_r < M.ncta && M.ng[0] > 1) || (M.rows_r > 0 && M.ng[1] > 1)) P.part_bufs = 2;
         // stages of this member's largest CTA
         P.stages = std::max<int64_t>(P.stages, (int64_t)M.ng[M.rows_r > 0 ? 1 : 0] *
                                                    ((nb + M.kb - 1) / M.kb));
@@ -150,7 +161,10 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
             P.x_bytes = std::max<int64_t>(P.x_bytes, (int64_t)ntok * nb * kq::rec_bytes(m.fmt == KQ_Q6_K));
         P.part_bytes = std::max<int64_t>(P.part_bytes, (int64_t)M.hmax * part_row);
     }
-    P.part_bytes = 2 * round_up(P.part_bytes, 128);  // two row groups in flight
+    // two row groups in flight (dp4a launches always; tensor-core launches
+    // where a CTA has a second group)
+    if (!tc) P.part_bufs = 2;
+    P.part_bytes = P.part_bufs * round_up(P.part_bytes, 128);
     P.slot_bytes = round_up(P.slot_bytes, 128);
     P.x_bytes = round_up(P.x_bytes, 128);
     if (tc) P.scr_bytes = round_up((int64_t)kq::kStreamConsumers * kq::kTcScrBytes, 128);
@@ -218,6 +232,7 @@ extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, in
     *o++ = P.smem;
     *o++ = P.stages;
     *o++ = P.scr_bytes;
+    *o++ = P.part_bufs;
     for (int i = 0; i < n; ++i) {
         const kqplan::Member &M = P.m[i];
         const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],

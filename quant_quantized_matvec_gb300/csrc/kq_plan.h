@@ -34,6 +34,7 @@ struct Plan {
     int level = -1;        // geometry level taken (records in global: level 0 geometry)
     bool xsmem = false;    // input records in shared memory
     int64_t x_bytes = 0, part_bytes = 0, slot_bytes = 0, nslot = 0, stages = 0;
+    int part_bufs = 2;      // partial buffers (1 when no CTA has a second row group)
     int64_t scr_bytes = 0;  // tensor-core launches: the consumer warps' unit scratch
     int tc_noct = 0;        // tensor-core launches: octets of tokens (0: dp4a launch)
     int64_t smem = 0;      // dynamic shared memory of the launch
@@ -48,8 +49,9 @@ constexpr int64_t kCostQ6 = 32;
 // dp4a launches: ntok 1..8, records in shared memory when they fit.
 // Tensor-core launches (tc_noct = 1 or 2 octets of tokens, ntok up to
 // 8 * tc_noct): records in global memory, partials for 8 * tc_noct token
-// columns, and one unit scratch per consumer warp.  KQ_ERR_SHAPE when no
-// geometry fits (the caller then uses the direct-load kernel).
+// columns (one buffer when no CTA has a second row group), and one unit
+// scratch per consumer warp.  KQ_ERR_SHAPE when no geometry fits (the
+// caller then uses the direct-load kernel).
 kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out,
                       int tc_noct = 0);
 

@@ -160,16 +160,19 @@ __device__ __forceinline__ void tc_a_from_bytes(uint32_t wa, uint32_t wb, uint32
 }
 
 // One unit.  Rows r of the tile at rowp(r) (r < nvalid), one block column,
-// NOCT octets of tokens; `frag` = fragments of (octet 0, this column),
-// `ostride` bytes between octets, `aux` = aux of (token 0, this column),
-// `taux` floats between tokens, `ntok` the launch's token columns.
-// Returns v[o][k2][j] for row g + 8 k2 and token 8o + 2t + j in lane
-// (g, t); tokens past ntok are garbage and not to be stored.
-template <int FMT, int NOCT, bool GW, class RowP>
-__device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *frag,
-                                        int64_t ostride, const float *aux, int64_t taux,
-                                        int ntok, float *scr, int lane,
-                                        float (&v)[NOCT][2][2]) {
+// NOCT octets of tokens; `col` = this column's input records (kq_xtc.cuh:
+// the fragments of octets 0..NOCT-1, then the aux of tokens 0..8 NOCT - 1),
+// in global memory (GB) or shared memory; `ntok` the launch's token
+// columns.  GW: the weights are in global memory.  Returns v[o][k2][j] for
+// row g + 8 k2 and token 8o + 2t + j in lane (g, t); tokens past ntok are
+// garbage and not to be stored.
+template <int FMT, int NOCT, bool GW, bool GB, class RowP>
+__device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *col, int ntok,
+                                        float *scr, int lane, float (&v)[NOCT][2][2]) {
+    const uint8_t *frag = col;
+    constexpr int ostride = kTcFragOctBytes;
+    const float *aux = reinterpret_cast<const float *>(col + NOCT * kTcFragOctBytes);
+    constexpr int taux = kTcAuxFloats;
     tc_scales<FMT, GW>(rowp, nvalid, scr, lane);
     __syncwarp();
     const int g = lane >> 2, t = lane & 3;
@@ -223,7 +226,7 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *fr
                     float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        const uint4 b = tc_ld<true, uint4>(fo + tc_frag_offset(2 * s + hf, 0));
+                        const uint4 b = tc_ld<GB, uint4>(fo + tc_frag_offset(2 * s + hf, 0));
                         mma_f16(D, A[hf], b.x, b.y);  // hi
                         mma_f16(D, A[hf], b.z, b.w);  // lo
                     }
@@ -242,9 +245,9 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *fr
                 int tok = 8 * o + 2 * t + j;
                 tok = tok < ntok ? tok : ntok - 1;
                 const float *ax = aux + tok * taux;
-                const float4 s0 = tc_ld<true, float4>(ax + kTcAuxS32);
-                const float4 s1 = tc_ld<true, float4>(ax + kTcAuxS32 + 4);
-                const float u = tc_ld<true, float>(ax + kTcAuxU);
+                const float4 s0 = tc_ld<GB, float4>(ax + kTcAuxS32);
+                const float4 s1 = tc_ld<GB, float4>(ax + kTcAuxS32 + 4);
+                const float u = tc_ld<GB, float>(ax + kTcAuxU);
                 const float S[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
                 for (int k2 = 0; k2 < 2; ++k2) {
@@ -285,7 +288,7 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *fr
                     for (int o = 0; o < NOCT; ++o) {
                         const uint8_t *fo = fl + o * ostride;
                         float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        const uint4 b = tc_ld<true, uint4>(fo + tc_frag_offset(s, 0));
+                        const uint4 b = tc_ld<GB, uint4>(fo + tc_frag_offset(s, 0));
                         mma_f16(D, A, b.x, b.y);  // hi
                         mma_f16(D, A, b.z, b.w);  // lo
                         acc[o][0][0] = fmaf(fa, D[0], acc[o][0][0]);
@@ -302,7 +305,7 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *fr
             for (int j = 0; j < 2; ++j) {
                 int tok = 8 * o + 2 * t + j;
                 tok = tok < ntok ? tok : ntok - 1;
-                const float u = tc_ld<true, float>(aux + tok * taux + kTcAuxU);
+                const float u = tc_ld<GB, float>(aux + tok * taux + kTcAuxU);
                 v[o][0][j] = u * acc[o][0][j];
                 v[o][1][j] = u * acc[o][1][j];
             }

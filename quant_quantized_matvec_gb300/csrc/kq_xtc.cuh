@@ -19,19 +19,22 @@
 // its column NaN, so that every output that reads the column is NaN.
 //
 // Records, in global memory, for `noct` octets of tokens (octet o holds
-// tokens 8o..8o+7; tokens past ntok are zero) and nb columns:
+// tokens 8o..8o+7; tokens past ntok are zero) and nb columns, one column
+// after another (tc_col_bytes(noct) each, so that the columns of a stage
+// are one contiguous copy):
 //
-//   fragments  [o][column][k][lane] x 16 bytes, k = 0..15 the k-step
-//              (inputs 16k..16k+15 of the column); lane L = 4g + t holds,
-//              for token 8o + g, the f16 pairs (hi[16k+4t], hi[16k+4t+2]),
+//   fragments  [o][k][lane] x 16 bytes, k = 0..15 the k-step (inputs
+//              16k..16k+15 of the column); lane L = 4g + t holds, for token
+//              8o + g, the f16 pairs (hi[16k+4t], hi[16k+4t+2]),
 //              (hi[16k+4t+1], hi[16k+4t+3]), then the same two pairs of lo
 //              -- the m16n8k16 B layout with the k index permuted (k-slot
 //              2t <-> input 4t, 2t+1 <-> 4t+2, 2t+8 <-> 4t+1, 2t+9 <->
 //              4t+3; the A side uses the same order), hi and lo side by
 //              side so that one 16-byte load fetches both
-//   aux        [token][column] x kTcAuxFloats: S32[0..7], the f32 sums of
-//              hi + lo over the 32-input sub-blocks in a fixed order (the
-//              Q4_K / Q5_K min term); then u.
+//   aux        [token 0..8 noct - 1] x kTcAuxFloats: S32[0..7], the f32 sums
+//              of hi + lo over the 32-input sub-blocks in a fixed order (the
+//              Q4_K / Q5_K min term); then u.  Tokens past ntok are not
+//              written and never read.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -41,18 +44,18 @@ namespace kq {
 
 constexpr int kTcMinNtok = 5;   // calls with at least this many token columns
 constexpr int kTcMaxOct = 2;    // octets of tokens per launch (16 tokens)
-constexpr int kTcFragColBytes = 16 * 32 * 16;  // one octet x one column
-constexpr int kTcAuxFloats = 16;
+constexpr int kTcFragOctBytes = 16 * 32 * 16;  // one octet of one column
+constexpr int kTcAuxFloats = 16;                // per token of one column
 constexpr int kTcAuxS32 = 0;
 constexpr int kTcAuxU = 8;
 
-__host__ __device__ constexpr int64_t tc_frag_bytes(int noct, int nb) {
-    return (int64_t)noct * nb * kTcFragColBytes;
+__host__ __device__ constexpr int tc_col_bytes(int noct) {
+    return noct * (kTcFragOctBytes + 8 * kTcAuxFloats * 4);
 }
 __host__ __device__ constexpr int64_t tc_record_bytes(int ntok, int nb) {
-    return tc_frag_bytes((ntok + 7) / 8, nb) + (int64_t)ntok * nb * kTcAuxFloats * 4;
+    return (int64_t)nb * tc_col_bytes((ntok + 7) / 8);
 }
-// Byte offset of (k-step, lane) inside one octet x column.
+// Byte offset of (k-step, lane) inside one octet of one column.
 __host__ __device__ __forceinline__ int tc_frag_offset(int k, int lane) {
     return (k * 32 + lane) * 16;
 }
@@ -64,7 +67,7 @@ __device__ __forceinline__ uint32_t half2_bits(__half a, __half b) {
 // The records of one octet o and one column j, k-steps 4q..4q+3 (q = 0..3:
 // four warps share a column; each takes the column's maximum itself), built
 // by one warp.  x is [ntok][nb * 256]; `frag` points at this (octet,
-// column)'s fragments and `aux` at the aux array of token 0, column 0.
+// column)'s fragments and `aux` at the column's aux of token 0.
 constexpr int kTcPrepSplit = 4;
 
 __device__ __forceinline__ void build_tc_record(const float *x, int ntok, int nb, int o, int j,
@@ -121,7 +124,7 @@ __device__ __forceinline__ void build_tc_record(const float *x, int ntok, int nb
         s16[kk] = part;
     }
     if (live && t == 0) {
-        float *a = aux + ((int64_t)tok * nb + j) * kTcAuxFloats;
+        float *a = aux + tok * kTcAuxFloats;
         *reinterpret_cast<float2 *>(a + kTcAuxS32 + 2 * q) =
             make_float2(s16[0] + s16[1], s16[2] + s16[3]);
         if (q == 0) a[kTcAuxU] = u;

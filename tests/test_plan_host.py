@@ -11,7 +11,7 @@ import pytest
 
 from quant_quantized_matvec_gb300 import _binding
 
-HEAD, MEMBER = 11, 20
+HEAD, MEMBER = 12, 20
 TC_MIN = 5                      # ntok from which the tensor-core path runs
 TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps
 SMS, SMEM = 152, 232448          # GB300: SMs, opt-in shared memory per CTA
@@ -30,7 +30,8 @@ def plan(members, ntok, sms=SMS, smem=SMEM):
     assert lib.kq_plan_describe(arr, len(members), ntok, sms, smem, out, len(out)) == 0
     o = list(out)
     head = dict(zip(["status", "grid", "level", "xsmem", "x_bytes", "part_bytes",
-                     "slot_bytes", "nslot", "smem", "stages", "scr_bytes"], o[:HEAD]))
+                     "slot_bytes", "nslot", "smem", "stages", "scr_bytes", "part_bufs"],
+                    o[:HEAD]))
     keys = ["ncta", "cta_begin", "rows_q", "rows_r", "ng0", "gq0", "gr0", "ng1", "gq1",
             "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes"]
     mem = [dict(zip(keys, o[HEAD + MEMBER * i: HEAD + MEMBER * (i + 1)]))
@@ -78,11 +79,18 @@ def check(members, ntok, sms=SMS, smem=SMEM):
             # a segment holds kb blocks plus up to 14 bytes of misalignment
             # at each end, and is an odd number of 16-byte units
             assert m["seg"] >= m["kb"] * 210 + 28 and m["seg"] % 16 == 0 and (m["seg"] // 16) % 2 == 1
-            assert h["slot_bytes"] >= m["hmax"] * m["seg"]
+            wpart = m["hmax"] * m["seg"]
         else:
-            assert m["seg"] == 0 and h["slot_bytes"] >= m["hmax"] * m["kb"] * BB[fmt]
+            assert m["seg"] == 0
             assert (m["kb"] * BB[fmt]) % 8 == 0  # tensor-map box rows in u64
-        assert h["part_bytes"] >= 2 * m["hmax"] * nb * ntp * 4
+            wpart = m["hmax"] * m["kb"] * BB[fmt]
+        assert h["slot_bytes"] >= wpart
+        # two partial buffers unless no CTA has a second row group
+        occurs = [m["rows_r"] < m["ncta"], m["rows_r"] > 0]
+        if any(m[f"ng{big}"] > 1 for big in (0, 1) if occurs[big]):
+            assert h["part_bufs"] == 2
+        assert h["part_bufs"] in (1, 2) and (h["part_bufs"] == 2 or ntok >= TC_MIN)
+        assert h["part_bytes"] >= h["part_bufs"] * m["hmax"] * nb * ntp * 4
         if h["xsmem"]:
             assert h["x_bytes"] >= ntok * nb * REC[fmt]
     assert begin == h["grid"]
