@@ -38,7 +38,7 @@
  *     allocations are stream-ordered temporaries (cudaMallocAsync /
  *     cudaFreeAsync on `stream`): the input records of calls whose records
  *     do not fit in shared memory, the tensor-core fragments of calls of 5
- *     or more token columns (about 8 KB per 256 inputs per group of 8
+ *     or more token columns (8704 bytes per 256 inputs per group of 8
  *     columns), and staged host inputs; kq_matvec_noalloc allocates
  *     nothing.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
@@ -297,8 +297,8 @@ int kq_last_launch_count(void);
  * stream-ordered temporary.  Calls whose records need more return
  * KQ_ERR_LIMIT with nothing enqueued: for ntok = 1..4, ntok * (cols / 256)
  * * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K; for ntok = 5..16
- * (tensor cores), ceil(ntok / 8) * (cols / 256) * 8192 bytes of fragments
- * plus ntok * (cols / 256) * 64 bytes, each plane rounded up to 256 bytes.
+ * (tensor cores), ceil(ntok / 8) * (cols / 256) * 8704 bytes of fragments,
+ * rounded up to 256 bytes.
  * The records are written in full before they are read, so nothing in the
  * buffer has to start at zero.
  *

@@ -173,6 +173,19 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
     constexpr int ostride = kTcFragOctBytes;
     const float *aux = reinterpret_cast<const float *>(col + NOCT * kTcFragOctBytes);
     constexpr int taux = kTcAuxFloats;
+    // One octet from global memory: all 16 k-steps' B fragments are
+    // requested before anything else, so that the unit waits on L2 once
+    // rather than once per sub-block.
+    constexpr bool PRE = GB && NOCT == 1;
+    uint4 bpre[PRE ? 16 : 1];
+    if constexpr (PRE) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) bpre[k] = tc_ld<true, uint4>(col + tc_frag_offset(k, lane));
+    }
+    auto bfrag = [&](const uint8_t *fo, int k) -> uint4 {
+        if constexpr (PRE) return bpre[k];
+        return tc_ld<GB, uint4>(fo + tc_frag_offset(k, 0));
+    };
     tc_scales<FMT, GW>(rowp, nvalid, scr, lane);
     __syncwarp();
     const int g = lane >> 2, t = lane & 3;
@@ -226,7 +239,7 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
                     float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        const uint4 b = tc_ld<GB, uint4>(fo + tc_frag_offset(2 * s + hf, 0));
+                        const uint4 b = bfrag(fo, 2 * s + hf);
                         mma_f16(D, A[hf], b.x, b.y);  // hi
                         mma_f16(D, A[hf], b.z, b.w);  // lo
                     }
@@ -288,7 +301,7 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
                     for (int o = 0; o < NOCT; ++o) {
                         const uint8_t *fo = fl + o * ostride;
                         float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        const uint4 b = tc_ld<GB, uint4>(fo + tc_frag_offset(s, 0));
+                        const uint4 b = bfrag(fo, s);
                         mma_f16(D, A, b.x, b.y);  // hi
                         mma_f16(D, A, b.z, b.w);  // lo
                         acc[o][0][0] = fmaf(fa, D[0], acc[o][0][0]);

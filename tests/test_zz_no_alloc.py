@@ -103,10 +103,10 @@ def test_noalloc_reads_pinned_host_x_in_place():
 def test_noalloc_rejects_records_beyond_its_buffer():
     lib = _binding.load()
     ntok, fmt = 8, kq.Q6_K
-    # tensor-core fragments of one octet, 8192 bytes per 256 inputs, plus
-    # 64 bytes per token and 256 inputs, above 1 MiB  ->  cols = 256 * 125
+    # tensor-core records of one octet, 8704 bytes per 256 inputs, above
+    # 1 MiB  ->  cols = 256 * 125
     cols = 256 * 125
-    assert (cols // 256) * (8192 + ntok * 64) > NOALLOC_RECORD_BYTES
+    assert (cols // 256) * 8704 > NOALLOC_RECORD_BYTES
     rows = 2
     W, x = C.case(fmt, rows, cols, ntok, "noalloc/limit")
     Wd, xd = C.to_dev(W), C.to_dev(x)
