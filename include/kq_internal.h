@@ -20,7 +20,7 @@ extern "C" {
 
 /*
  * The streaming kernel's launch geometry for the set `mats` (n members,
- * ntok token columns in the launch: 1..4 for the dp4a kernels, 5..16 for
+ * ntok token columns in the launch: 1..3 for the dp4a kernels, 4..16 for
  * the tensor-core kernels, as the library chooses) on a device with `sms` SMs and
  * `smem_optin` bytes of opt-in shared memory per CTA, as the library would
  * plan it.  Pure host arithmetic on the descriptors' shapes and formats

@@ -42,7 +42,7 @@
 
 namespace kq {
 
-constexpr int kTcMinNtok = 5;   // calls with at least this many token columns
+constexpr int kTcMinNtok = 4;   // calls with at least this many token columns
 constexpr int kTcMaxOct = 2;    // octets of tokens per launch (16 tokens)
 constexpr int kTcFragOctBytes = 16 * 32 * 16;  // one octet of one column
 constexpr int kTcAuxFloats = 16;                // per token of one column

@@ -16,7 +16,7 @@ when the outlier sits on a zero weight.  Cases:
   * one input of 1e4 on a zero weight in every row: within the contract;
   * one input of 1e6 on a zero weight in every row: outside the contract,
     as include/kq.h states, but within the contract widened by B.
-Calls of 5 or more token columns run on the tensor cores instead, where
+Calls of 4 or more token columns run on the tensor cores instead, where
 each input keeps about 22 significant bits and the rounding floor is
 2^(E - 39) for a 256-input column whose largest magnitude is below 2^E
 (kq_xtc.cuh): there every case above, the 1e6 outlier included, is within

@@ -12,7 +12,7 @@ import pytest
 from quant_quantized_matvec_gb300 import _binding
 
 HEAD, MEMBER = 12, 20
-TC_MIN = 5                      # ntok from which the tensor-core path runs
+TC_MIN = 4                      # ntok from which the tensor-core path runs
 TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps
 SMS, SMEM = 152, 232448          # GB300: SMs, opt-in shared memory per CTA
 BB = {12: 144, 13: 176, 14: 210}

@@ -7,7 +7,9 @@ the waits expire on purpose.  The kernel must then report, not hang: the
 call returns, the device error word reads KQ_ERR_TIMEOUT, every output is
 either NaN (rows the CTA could not finish) or correct, the copies it had
 issued have landed (the next calls on the same SMs compute normally), and a
-call made with the default limit matches the oracle again.
+call made with the default limit matches the oracle again.  Both
+arithmetics are covered: one token column (dp4a) and eight (the tensor-core
+launch, after its fragment pass).
 """
 import numpy as np
 import pytest
@@ -44,17 +46,18 @@ def _nan_or_correct(fmt, W, rows, cols, x, y):
     return int(nan.sum())
 
 
+@pytest.mark.parametrize("ntok", [1, 8])
 @pytest.mark.parametrize("limit_ns", [1, 200])
-def test_expired_waits_are_reported_and_the_next_call_is_correct(limit_ns):
+def test_expired_waits_are_reported_and_the_next_call_is_correct(limit_ns, ntok):
     lib = _binding.load()
     assert not kq.device_error(clear=True)
-    ntok, cols = 1, 6656
+    cols = 6656
     shapes = [(kq.Q4_K, 4096), (kq.Q6_K, 256), (kq.Q6_K, 256), (kq.Q4_K, 4096)]
-    x = C.case(kq.Q4_K, 1, cols, ntok, "expiry/x")[1]
+    x = C.case(kq.Q4_K, 1, cols, ntok, f"expiry/x/{ntok}")[1]
     xd = C.to_dev(x)
     host, members = [], []
     for i, (fmt, rows) in enumerate(shapes):
-        W, _ = C.case(fmt, rows, cols, ntok, f"expiry/W{i}")
+        W, _ = C.case(fmt, rows, cols, 1, f"expiry/W{i}")
         g = C.Guarded(ntok, rows)
         host.append((fmt, W, rows, g))
         members.append((fmt, C.to_dev(W), rows, cols, xd, g.y))
