@@ -16,7 +16,7 @@ extern "C" {
 /* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
  * KQ_PLAN_MEMBER per member. */
 #define KQ_PLAN_HEAD 12
-#define KQ_PLAN_MEMBER 20
+#define KQ_PLAN_MEMBER 21
 
 /*
  * The streaming kernel's launch geometry for the set `mats` (n members,
@@ -35,7 +35,8 @@ extern "C" {
  *   [11] partial buffers (2; 1 for a tensor-core launch whose CTAs have
  *   one row group each)
  *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
- *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes.
+ *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes, whole (Q6_K
+ *   stages of whole rows, one bulk copy each: 1; else 0).
  * Returns 0, or -1 for bad arguments (nothing written).
  */
 int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,

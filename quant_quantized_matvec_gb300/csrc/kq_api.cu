@@ -513,6 +513,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         M.rmax = Q.rmax;
         M.kb = Q.kb;
         M.seg = Q.seg;
+        M.q6_whole = Q.whole;
         M.nmaps = m.fmt == KQ_Q6_K ? 0 : Q.nh;
         if (m.fmt != KQ_Q6_K) {
             // one tensor map per group height: boxes [h][kb * BB / 8] of u64
@@ -732,6 +733,7 @@ kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         M.rmax = Q.rmax;
         M.kb = Q.kb;
         M.seg = Q.seg;
+        M.q6_whole = Q.whole;
         M.nmaps = m.fmt == KQ_Q6_K ? 0 : Q.nh;
         if (m.fmt != KQ_Q6_K) {
             const int box_w = (int)(Q.kb * block_bytes_of(m.fmt) / 8);

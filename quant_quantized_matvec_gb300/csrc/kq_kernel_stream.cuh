@@ -65,6 +65,7 @@ struct StreamMember {
     int32_t rmax;   // rows per group at most
     int32_t kb;     // blocks per stage row
     int32_t seg;    // Q6_K: bytes between row segments in a slot
+    int32_t q6_whole;  // Q6_K: stages of whole rows, one bulk copy each
     int32_t nmaps;  // tensor maps (box heights) for this member (Q4_K / Q5_K)
     int32_t map_h[kMaxMaps];
 };
@@ -210,6 +211,18 @@ struct Groups {
     }
 };
 
+// Offset in a Q6_K stage slot of row r's block column b0 (`base` = the
+// stage's first row's byte offset in W plus 210 b0; rows `rb` bytes long).
+// Whole-row stages are one copy from the 16-byte boundary at or below the
+// first row, so row r sits at (base mod 16) + r rb; row segments are
+// `seg` bytes apart, each starting as far past a 16-byte boundary as its
+// first block does in memory (the low four bits survive wrap-around).
+__device__ __forceinline__ uint32_t q6_row_off(uint32_t base, int r, uint32_t rb, int seg,
+                                               bool whole) {
+    return whole ? (base & 15u) + (uint32_t)r * rb
+                 : (uint32_t)(r * seg) + ((base + (uint32_t)r * rb) & 15u);
+}
+
 // Row pairs of a stage of h rows: rows p and p + hp for p < hp.
 __device__ __forceinline__ int pair_offset(int h) { return (h + 1) >> 1; }
 
@@ -235,6 +248,7 @@ struct ConsumerCtx {
     int nb, kb, nbox, nstage;
     int64_t rows, row_bytes;
     int q6_seg;
+    bool q6_whole;
     float *y;
     Groups G;
     int *abort_flag;
@@ -352,10 +366,9 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                     // block start (row g0 + r, block b0) mod 16: the low four
                     // bits survive 32-bit wrap-around
                     const uint32_t base = (uint32_t)g0 * (uint32_t)c.row_bytes + (uint32_t)b0 * 210u;
-                    const uint32_t m0 = (base + (uint32_t)r * (uint32_t)c.row_bytes) & 15u;
-                    const uint32_t m1 = (base + (uint32_t)r2 * (uint32_t)c.row_bytes) & 15u;
-                    const uint8_t *a0 = sdp + r * c.q6_seg + m0 + j * 210;
-                    const uint8_t *a1 = sdp + r2 * c.q6_seg + m1 + j * 210;
+                    const uint32_t rb = (uint32_t)c.row_bytes;
+                    const uint8_t *a0 = sdp + q6_row_off(base, r, rb, c.q6_seg, c.q6_whole) + j * 210;
+                    const uint8_t *a1 = sdp + q6_row_off(base, r2, rb, c.q6_seg, c.q6_whole) + j * 210;
                     Q6WordsShared W[R];
                     W[0] = Q6WordsShared::at(a0);
                     if (R == 2) W[R - 1] = Q6WordsShared::at(a1);
@@ -484,8 +497,7 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
                 const uint32_t rb = (uint32_t)c.row_bytes;
                 tc_unit<FMT, NOCT, false, true>(
                     [&](int r) {
-                        const uint32_t m = (base + (uint32_t)(r0 + r) * rb) & 15u;
-                        return sdp + (r0 + r) * c.q6_seg + m + j * 210;
+                        return sdp + q6_row_off(base, r0 + r, rb, c.q6_seg, c.q6_whole) + j * 210;
                     },
                     nvalid, col, c.ntok, scr, lane, v);
             }
@@ -661,6 +673,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     mbar_expect_tx(full, (uint32_t)(h * box_row));
                     tensor2d_g2s(dst, &p.maps[mi][mj], k * (box_row / 8), (int)g0, full);
                 }
+            } else if (M.q6_whole) {
+                // one 16-byte-aligned bulk copy of the stage's whole rows;
+                // the sub-16-byte tail at the very end of the matrix is
+                // copied with plain loads
+                if (lane == 0) {
+                    const int64_t total = M.rows * row_bytes;
+                    const int64_t a = g0 * row_bytes, e = (g0 + h) * row_bytes;
+                    const int64_t a16 = a & ~(int64_t)15;
+                    int64_t e16 = (e + 15) & ~(int64_t)15;
+                    if (e16 > total) {
+                        e16 = total & ~(int64_t)15;
+                        uint8_t *dstp = smem + (dst - bars);
+                        for (int64_t i = e16; i < e; ++i) dstp[i - a16] = M.W[i];
+                    }
+                    // the tail's plain stores precede this arrive (a release)
+                    mbar_expect_tx(full, (uint32_t)(e16 - a16));
+                    bulk_g2s(dst, M.W + a16, (uint32_t)(e16 - a16), full);
+                }
             } else {
                 // one 16-byte-aligned bulk copy per row segment (blocks
                 // b0..b0+kbv of the row), segments M.seg bytes apart; the
@@ -747,6 +777,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.rows = M.rows;
     c.row_bytes = row_bytes;
     c.q6_seg = M.seg;
+    c.q6_whole = M.q6_whole != 0;
     c.y = M.y;
     c.G = G;
     c.abort_flag = &abort_flag;

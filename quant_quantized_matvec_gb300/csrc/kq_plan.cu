@@ -70,6 +70,14 @@ int64_t stage_weight_bytes(int fmt, int h, int kb) {
     return fmt == KQ_Q6_K ? (int64_t)h * q6_seg(kb) : (int64_t)h * kb * block_bytes(fmt);
 }
 
+// Q6_K rows of at most this many bytes are staged whole: a stage is a run
+// of consecutive rows, one contiguous bulk copy (their bytes plus up to 15
+// before and after for 16-byte alignment).  Longer rows are staged in
+// per-row segments of kb blocks, so that a stage still holds enough rows.
+constexpr int64_t kQ6WholeRowMax = 8192;
+
+int64_t q6_whole_bytes(int h, int64_t row_bytes) { return round_up(h * row_bytes + 30, 16); }
+
 // Stage geometry levels, from the largest stages down: stages are
 // [h rows][kb blocks] with h <= rcap and stage rows of at most kb_bytes.
 constexpr int kLevelRcap[] = {32, 16, 16, 8, 8};
@@ -98,8 +106,26 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
         cta += ncta[i];
         // rows per group: partials for the group must fit in 64 KiB
         const int64_t part_row = (int64_t)nb * ntok_part * 4;
-        const int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
+        int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
         if (rmax < 1) return KQ_ERR_SHAPE;
+        // Whole Q6_K rows (dp4a launches): a stage is one group of about
+        // kb_bytes x rcap bytes of consecutive rows.  Taken when a CTA's
+        // rows fit in one such stage, or are more than one group of row
+        // segments anyway; in between, whole-row stages would split a
+        // single segment group into several (measured slower at 27 rows
+        // per CTA: 9.20 vs 8.44 us on Q6_K 4096x6656).  Tensor-core
+        // launches keep segments: their units read every stage's columns'
+        // input fragments, which whole-row stages of few rows would
+        // multiply.
+        if (!tc && m.fmt == KQ_Q6_K && M.row_bytes <= kQ6WholeRowMax) {
+            const int hw = (int)std::max<int64_t>(
+                1, std::min<int64_t>(rmax, (int64_t)kb_bytes * rcap / M.row_bytes));
+            const int64_t cta_rows = M.rows_q + (M.rows_r > 0 ? 1 : 0);
+            if (cta_rows <= hw || cta_rows > rmax) {
+                M.whole = 1;
+                rmax = hw;
+            }
+        }
         M.rmax = rmax;
         for (int big = 0; big < 2; ++big) {  // CTAs of rows_q / rows_q + 1 rows
             const int64_t nn = M.rows_q + big;
@@ -140,7 +166,7 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
                 }
             }
             if (best == 0) return KQ_ERR_SHAPE;
-            M.kb = best;
+            M.kb = M.whole ? nb : best;
         }
         // dp4a launches: tasks of a stage (row pairs x block columns) stay
         // below 2^12, the range of the kernel's multiply-shift division
@@ -148,8 +174,10 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
             const int hp = kq::stream_rows_per_task(m.fmt, ntok) == 2 ? (M.hmax + 1) / 2 : M.hmax;
             if ((int64_t)hp * M.kb >= 4096) return KQ_ERR_SHAPE;
         }
-        if (m.fmt == KQ_Q6_K) M.seg = q6_seg(M.kb);
-        P.slot_bytes = std::max<int64_t>(P.slot_bytes, stage_weight_bytes(m.fmt, M.hmax, M.kb));
+        if (m.fmt == KQ_Q6_K) M.seg = M.whole ? (int)M.row_bytes : q6_seg(M.kb);
+        P.slot_bytes = std::max<int64_t>(
+            P.slot_bytes, M.whole ? q6_whole_bytes(M.hmax, M.row_bytes)
+                                  : stage_weight_bytes(m.fmt, M.hmax, M.kb));
         // CTAs of rows_q (+ 1) rows exist when rows_r < ncta (rows_r > 0)
         if ((M.rows_r < M.ncta && M.ng[0] > 1) || (M.rows_r > 0 && M.ng[1] > 1)) P.part_bufs = 2;
         // stages of this member's largest CTA
@@ -238,7 +266,8 @@ extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, in
         const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],
                                            M.gq[0], M.gr[0], M.ng[1], M.gq[1], M.gr[1],
                                            M.rmax, M.kb, M.seg, M.hmax, M.nh, M.hs[0],
-                                           M.hs[1], M.hs[2], M.hs[3], M.row_bytes};
+                                           M.hs[1], M.hs[2], M.hs[3], M.row_bytes,
+                                           M.whole};
         for (int k = 0; k < KQ_PLAN_MEMBER; ++k) *o++ = v[k];
     }
     return 0;

@@ -24,6 +24,7 @@ struct Member {
     int rmax = 0;                     // rows per group at most
     int kb = 0;                       // blocks per stage row
     int seg = 0;                      // Q6_K: bytes between row segments in a slot
+    int whole = 0;                    // Q6_K: stages of whole rows (one copy each)
     int nh = 0, hs[kMaxHeights] = {}; // group heights that occur
     int hmax = 0;
     int64_t row_bytes = 0;

@@ -11,7 +11,7 @@ import pytest
 
 from quant_quantized_matvec_gb300 import _binding
 
-HEAD, MEMBER = 12, 20
+HEAD, MEMBER = 12, 21
 TC_MIN = 4                      # ntok from which the tensor-core path runs
 TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps
 SMS, SMEM = 152, 232448          # GB300: SMs, opt-in shared memory per CTA
@@ -33,7 +33,8 @@ def plan(members, ntok, sms=SMS, smem=SMEM):
                      "slot_bytes", "nslot", "smem", "stages", "scr_bytes", "part_bufs"],
                     o[:HEAD]))
     keys = ["ncta", "cta_begin", "rows_q", "rows_r", "ng0", "gq0", "gr0", "ng1", "gq1",
-            "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes"]
+            "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes",
+            "whole"]
     mem = [dict(zip(keys, o[HEAD + MEMBER * i: HEAD + MEMBER * (i + 1)]))
            for i in range(len(members))]
     return head, mem
@@ -72,15 +73,24 @@ def check(members, ntok, sms=SMS, smem=SMEM):
         # for 8 or 16 token columns)
         ntp = 8 * ((ntok + 7) // 8) if ntok >= TC_MIN else ntok
         assert m["hmax"] * nb * ntp * 4 <= 64 * 1024
-        # stage rows: at most 2048 bytes, tasks below 2^12
-        assert 1 <= m["kb"] <= nb and m["kb"] * BB[fmt] <= 2048
+        # stage rows: at most 2048 bytes (whole Q6_K rows: up to 8 KB),
+        # tasks below 2^12
         assert ((m["hmax"] + 1) // 2) * m["kb"] < 4096
-        if fmt == 14:
+        # whole Q6_K rows only in dp4a launches of rows up to 8 KB
+        assert not m["whole"] or (fmt == 14 and m["row_bytes"] <= 8192 and ntok < TC_MIN)
+        if m["whole"]:
+            # consecutive whole rows, one copy from the 16-byte boundary at
+            # or below the first row to the one at or above the last byte
+            assert m["kb"] == nb and m["seg"] == m["row_bytes"]
+            wpart = m["hmax"] * m["row_bytes"] + 30
+        elif fmt == 14:
+            assert 1 <= m["kb"] <= nb and m["kb"] * BB[fmt] <= 2048
             # a segment holds kb blocks plus up to 14 bytes of misalignment
             # at each end, and is an odd number of 16-byte units
             assert m["seg"] >= m["kb"] * 210 + 28 and m["seg"] % 16 == 0 and (m["seg"] // 16) % 2 == 1
             wpart = m["hmax"] * m["seg"]
         else:
+            assert 1 <= m["kb"] <= nb and m["kb"] * BB[fmt] <= 2048
             assert m["seg"] == 0
             assert (m["kb"] * BB[fmt]) % 8 == 0  # tensor-map box rows in u64
             wpart = m["hmax"] * m["kb"] * BB[fmt]
