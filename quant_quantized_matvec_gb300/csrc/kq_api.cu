@@ -582,6 +582,20 @@ int tc_enabled() {
     return c;
 }
 
+// The arithmetic of a member: the tensor cores for kq::kTcMinNtok or more
+// token columns, and for 2 or 3 when the member's dp4a input records
+// (ntok x nb x record bytes) would pass kTcRecordBytes and so not stay in
+// shared memory (wide matrices: FFN down, draft fc); else dp4a.  A function
+// of the format, the columns and ntok alone, so that a set and separate
+// calls, or row shards and the whole matrix, choose alike.
+constexpr int64_t kTcRecordBytes = 140 * 1024;
+bool member_tc(const kq_mat &m, int ntok) {
+    if (!tc_enabled()) return false;
+    if (ntok >= kq::kTcMinNtok) return true;
+    return ntok >= 2 &&
+           (int64_t)ntok * (m.cols / 256) * kq::rec_bytes(m.fmt == KQ_Q6_K) > kTcRecordBytes;
+}
+
 // Tensor-core records (kq_xtc.cuh) of every member in `buf` (caller-
 // provided, or a stream-ordered temporary when buf is null: *owned is then
 // set), one per distinct input plane; rec[i]: member i's records.
@@ -931,21 +945,26 @@ kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
     const bool after = staged != nullptr;
     int kernels = 0, launches = after ? 1 : 0;
     kq_status st = KQ_OK;
-    if (ntok >= kq::kTcMinNtok && tc_enabled()) {
-        st = run_tc(mats, n, ntok, s);
+    // members by arithmetic: normally all alike (one launch); a set that
+    // mixes them runs as one launch per arithmetic
+    kq_mat tcm[KQ_MAX_SET], dpm[KQ_MAX_SET];
+    int ntc = 0, ndp = 0;
+    for (int i = 0; i < n; ++i) (member_tc(mats[i], ntok) ? tcm[ntc++] : dpm[ndp++]) = mats[i];
+    if (ntc > 0) {
+        st = run_tc(tcm, ntc, ntok, s);
         kernels = g_last_kernels;
         launches += g_last_launches;
     }
     const int cn = launch_ntok();
     // dp4a: near-equal chunks, the first `rem` taking one column more
-    const int nch = (ntok >= kq::kTcMinNtok && tc_enabled()) ? 0 : (ntok + cn - 1) / cn;
+    const int nch = ndp > 0 ? (ntok + cn - 1) / cn : 0;
     const int base = nch ? ntok / nch : 0, rem = nch ? ntok % nch : 0;
     kq_mat part[KQ_MAX_SET];
     for (int ci = 0, t0 = 0; ci < nch && st == KQ_OK; ++ci) {
         const int nt = base + (ci < rem ? 1 : 0);
-        token_chunk(mats, n, t0, part);
+        token_chunk(dpm, ndp, t0, part);
         t0 += nt;
-        st = run_chunk(part, n, nt, stream, after);
+        st = run_chunk(part, ndp, nt, stream, after);
         kernels |= g_last_kernels;
         launches += g_last_launches;
     }
@@ -1014,7 +1033,7 @@ kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
     // ntok columns, or the dp4a records of at most kLaunchNtok columns
     const int nb = (int)(in.cols / 256);
     const bool q6 = in.fmt == KQ_Q6_K;
-    const bool tc = ntok >= kq::kTcMinNtok && tc_enabled();
+    const bool tc = member_tc(in, ntok);
     const int64_t rec_total = tc ? tc_records_bytes(&in, 1, ntok)
                                  : (int64_t)std::min(ntok, kLaunchNtok) * nb * kq::rec_bytes(q6);
     if (rec_total > KQ_NOALLOC_RECORD_BYTES) return KQ_ERR_LIMIT;

@@ -124,3 +124,52 @@ def test_noalloc_ntok12_equals_kq_matvec():
     assert np.array_equal(bits(a.host()), bits(b.host()))
     C.check(fmt, W, rows, cols, x, a.host(), what="noalloc ntok=12")
     assert not kq.device_error()
+
+
+@pytest.mark.parametrize("ntok", [2, 3])
+@pytest.mark.parametrize("fmt,cols", [(kq.Q6_K, 19968), (kq.Q4_K, 33280)])
+def test_wide_matrices_take_the_tensor_cores_from_two_columns(fmt, cols, ntok):
+    """At 2 or 3 token columns a matrix whose dp4a input records would not
+    stay in shared memory (ntok x cols/256 x record bytes above 140 KB) runs
+    on the tensor cores; a narrow one stays on dp4a.  Both match the
+    oracle."""
+    rows = 200
+    W, x = C.case(fmt, rows, cols, ntok, f"wide/{fmt}/{ntok}")
+    g = C.Guarded(ntok, rows)
+    kq.matvec(fmt, C.to_dev(W), rows, cols, C.to_dev(x), y=g.y)
+    torch.cuda.synchronize()
+    rec = 1056 if fmt == kq.Q6_K else 832
+    assert kq.last_kernels()["tensor_cores"] == (ntok * (cols // 256) * rec > 140 * 1024)
+    C.check(fmt, W, rows, cols, x, g.host(), what=f"{NAMES[fmt]} {cols} ntok={ntok}")
+    Wn, xn = C.case(fmt, rows, 2560, ntok, f"narrow/{fmt}/{ntok}")
+    gn = C.Guarded(ntok, rows)
+    kq.matvec(fmt, C.to_dev(Wn), rows, 2560, C.to_dev(xn), y=gn.y)
+    torch.cuda.synchronize()
+    assert not kq.last_kernels()["tensor_cores"]
+    C.check(fmt, Wn, rows, 2560, xn, gn.host(), what=f"{NAMES[fmt]} 2560 ntok={ntok}")
+    assert not kq.device_error()
+
+
+def test_set_mixing_arithmetics_equals_separate_calls():
+    """A set at ntok 3 whose wide member runs on the tensor cores and whose
+    narrow members run on dp4a: one launch per arithmetic, every output
+    bitwise what a separate call writes."""
+    ntok = 3
+    specs = [(kq.Q4_K, 300, 2560, "a"), (kq.Q6_K, 160, 19968, "b"), (kq.Q5_K, 77, 6656, "c")]
+    members, seps, hosts = [], [], []
+    for fmt, rows, cols, tag in specs:
+        W, x = C.case(fmt, rows, cols, ntok, f"mix/{tag}")
+        Wd, xd = C.to_dev(W), C.to_dev(x)
+        gs, gp = C.Guarded(ntok, rows), C.Guarded(ntok, rows)
+        members.append((fmt, Wd, rows, cols, xd, gs.y))
+        kq.matvec(fmt, Wd, rows, cols, xd, y=gp.y)
+        seps.append(gp)
+        hosts.append((fmt, W, rows, cols, x, gs))
+    kq.matvec_set(members, ntok=ntok)
+    torch.cuda.synchronize()
+    lk = kq.last_kernels()
+    assert lk["tensor_cores"] and lk["stream"]
+    for (fmt, W, rows, cols, x, gs), gp in zip(hosts, seps):
+        assert np.array_equal(bits(gs.host()), bits(gp.host()))
+        C.check(fmt, W, rows, cols, x, gs.host(), what="mixed set ntok=3")
+    assert not kq.device_error()
