@@ -13,14 +13,19 @@
  *     Q5_K  176 B / block   w = d*sc_j*(nibble | hbit<<4) - dmin*m_j  (6.4)
  *     Q6_K  210 B / block   w = d*sc_j*(code - 32), 16 int8 scales   (6.5)
  *
- * x and y are f32.  A call of 1..3 token columns is one launch of the
- * integer (dp4a) kernels, all columns sharing one read of W.  A call of
- * 4..16 token columns runs on the tensor cores (mma.sync m16n8k16, f16
- * operands, f32 accumulation; "Chapter 6", section 6.8, the weight-
- * stationary tile for many columns): a short pass turns x into f16 operand
- * fragments, then one launch reads W once for all the columns.  A token
- * column's result depends on its own inputs and on which of the two
- * arithmetics the call's ntok selects -- never on the other columns.
+ * x and y are f32.  A matrix is computed with one of two arithmetics,
+ * chosen from its format, cols and ntok alone:
+ *   - integer (dp4a) block sums, for 1 token column, and for 2..3 unless
+ *     ntok x (cols / 256) x the record bytes (832 for Q4_K / Q5_K, 1056
+ *     for Q6_K) passes 140 KB;
+ *   - the tensor cores (mma.sync m16n8k16, f16 operands, f32 accumulation;
+ *     "Chapter 6", section 6.8, the weight-stationary tile for many
+ *     columns) otherwise, i.e. for 4..16 token columns and for wide
+ *     matrices at 2..3: a short pass turns x into f16 operand fragments,
+ *     then one launch reads W once for all the columns.
+ * A token column's result depends on its own inputs and on the arithmetic
+ * -- never on the other columns, the number of rows or the other members
+ * of a set (a set that mixes the two runs one launch per arithmetic).
  *
  * Conventions for every entry point below
  *   - W is a DEVICE pointer (cudaMalloc / torch CUDA storage on the current
@@ -37,10 +42,9 @@
  *     keeps no pointer after a call returns and never synchronizes.  Its
  *     allocations are stream-ordered temporaries (cudaMallocAsync /
  *     cudaFreeAsync on `stream`): the input records of calls whose records
- *     do not fit in shared memory, the tensor-core fragments of calls of 4
- *     or more token columns (8704 bytes per 256 inputs per group of 8
- *     columns), and staged host inputs; kq_matvec_noalloc allocates
- *     nothing.
+ *     do not fit in shared memory, the fragments of the tensor-core
+ *     arithmetic (8704 bytes per 256 inputs per group of 8 columns), and
+ *     staged host inputs; kq_matvec_noalloc allocates nothing.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream) and may be captured in a CUDA graph.
  *   - Every argument is validated on the host before anything is launched;
@@ -67,8 +71,8 @@
  *     hundreds of times inside it; an input of 1e6 on an exactly zero
  *     weight among N(0,1) inputs is about 10x outside it, though still
  *     within B.  NaN or infinite inputs make the outputs that read their
- *     group NaN.  This holds for calls of 1..3 token columns.
- *     Calls of 4..16 token columns (tensor cores) hold each input as two f16
+ *     group NaN.  This holds for the dp4a arithmetic.
+ *     The tensor-core arithmetic holds each input as two f16
  *     terms after scaling its 256-input column by a power of two: an input
  *     error of at most max(2^-22 |x_j|, 2^(E-39)), max|x| < 2^E over the
  *     column; codes times these terms are exact and the sums are f32.  The
@@ -269,7 +273,7 @@ int kq_set_overlap(int enable);
  * kq_matvec_set / kq_matvec_noalloc call enqueued, as bits: 1 = the direct-load kernel, 2 = the
  * TMA-streaming kernel, 4 = the pass that writes input records to global
  * memory first (when they do not fit in shared memory), 8 = the tensor-core
- * arithmetic (calls of 4 or more token columns, after their fragment pass).
+ * arithmetic (after its fragment pass).
  * 0 before any call.
  */
 int kq_last_kernels(void);
@@ -295,10 +299,10 @@ int kq_last_launch_count(void);
  * load kernel with its input records (see the record pass) in one fixed
  * file-scope device buffer of KQ_NOALLOC_RECORD_BYTES bytes instead of a
  * stream-ordered temporary.  Calls whose records need more return
- * KQ_ERR_LIMIT with nothing enqueued: for ntok = 1..3, ntok * (cols / 256)
- * * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K; for ntok = 4..16
- * (tensor cores), ceil(ntok / 8) * (cols / 256) * 8704 bytes of fragments,
- * rounded up to 256 bytes.
+ * KQ_ERR_LIMIT with nothing enqueued: with the dp4a arithmetic,
+ * ntok * (cols / 256) * 832 bytes for Q4_K / Q5_K, * 1056 bytes for Q6_K;
+ * with the tensor cores, ceil(ntok / 8) * (cols / 256) * 8704 bytes of
+ * fragments, rounded up to 256 bytes.
  * The records are written in full before they are read, so nothing in the
  * buffer has to start at zero.
  *

@@ -20,8 +20,9 @@ extern "C" {
 
 /*
  * The streaming kernel's launch geometry for the set `mats` (n members,
- * ntok token columns in the launch: 1..3 for the dp4a kernels, 4..16 for
- * the tensor-core kernels, as the library chooses) on a device with `sms` SMs and
+ * ntok token columns in the launch: the dp4a launch for 1..3, the
+ * tensor-core launch for 4..16; the library also runs a wide matrix at
+ * 2..3 on the tensor cores, see kq.h) on a device with `sms` SMs and
  * `smem_optin` bytes of opt-in shared memory per CTA, as the library would
  * plan it.  Pure host arithmetic on the descriptors' shapes and formats
  * (their pointers are not read).
