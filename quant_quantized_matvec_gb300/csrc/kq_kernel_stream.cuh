@@ -223,6 +223,11 @@ __device__ __forceinline__ uint32_t q6_row_off(uint32_t base, int r, uint32_t rb
                  : (uint32_t)(r * seg) + ((base + (uint32_t)r * rb) & 15u);
 }
 
+// Floats between rows of a partial buffer ([row][block][token]): one more
+// than a row's nb x nt, an odd count, so that reads of one token from
+// consecutive rows (the reductions) fall on distinct banks.
+__host__ __device__ __forceinline__ int part_row_floats(int nb, int nt) { return nb * nt + 1; }
+
 // Row pairs of a stage of h rows: rows p and p + hp for p < hp.
 __device__ __forceinline__ int pair_offset(int h) { return (h + 1) >> 1; }
 
@@ -275,7 +280,7 @@ __device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, 
 #pragma unroll 1
     for (int o = warp * 32 + lane; o < h * ntok; o += kStreamConsumers * 32) {
         const int tt = o / h, r = o - tt * h;
-        const float *pp = pbuf + (int64_t)r * nb * nt + tt;
+        const float *pp = pbuf + (int64_t)r * part_row_floats(nb, nt) + tt;
         float acc = pp[0];
 #pragma unroll 4
         for (int bb = 1; bb < nb; ++bb) acc += pp[bb * nt];
@@ -293,6 +298,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
     using XR = Rec<!XSMEM>;
     const int nb = c.nb;
     const int tstride = nb * REC;
+    const int prow = part_row_floats(nb, NTOK);
     if (XSMEM) {
         build_records<Q6>(c.x, (int64_t)nb * 256, NTOK, nb, c.recs_w, warp, kStreamConsumers,
                           lane, [&] {
@@ -377,8 +383,8 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                 if (valid) {
 #pragma unroll
                     for (int tt = 0; tt < NTOK; ++tt) {
-                        pbuf[(r * nb + b) * NTOK + tt] = part[0][tt];
-                        if (R == 2 && r2 != r) pbuf[(r2 * nb + b) * NTOK + tt] = part[R - 1][tt];
+                        pbuf[r * prow + b * NTOK + tt] = part[0][tt];
+                        if (R == 2 && r2 != r) pbuf[r2 * prow + b * NTOK + tt] = part[R - 1][tt];
                     }
                 }
             }
@@ -403,9 +409,9 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                 if (lane < h) {
 #pragma unroll 1
                     for (int tt = 0; tt < NTOK; ++tt) {
-                        float acc = pbuf[(lane * nb) * NTOK + tt];
+                        float acc = pbuf[lane * prow + tt];
 #pragma unroll 4
-                        for (int bb = 1; bb < nb; ++bb) acc += pbuf[(lane * nb + bb) * NTOK + tt];
+                        for (int bb = 1; bb < nb; ++bb) acc += pbuf[lane * prow + bb * NTOK + tt];
                         c.y[(int64_t)tt * c.rows + g0 + lane] =
                             bad ? __int_as_float(0x7FC00000) : acc;
                     }
@@ -449,6 +455,7 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
     constexpr bool Q6 = FMT == kFmtQ6K;
     constexpr int BB = Q6 ? 210 : (FMT == kFmtQ5K ? 176 : 144);
     const int nb = c.nb;
+    const int prow = part_row_floats(nb, NT);
     float *scr = c.scr + warp * (kTcScrBytes / 4);
     constexpr int colb = tc_col_bytes(NOCT);
     int next = warp;  // this warp's next unit, counted over the whole CTA
@@ -510,7 +517,7 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
                     for (int o = 0; o < NOCT; ++o)
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj)
-                            pbuf[(row * nb + b0 + j) * NT + 8 * o + 2 * t4 + jj] = v[o][k2][jj];
+                            pbuf[row * prow + (b0 + j) * NT + 8 * o + 2 * t4 + jj] = v[o][k2][jj];
                 }
             }
         }
@@ -532,9 +539,9 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
                 if (lane < h) {
 #pragma unroll 1
                     for (int tt = 0; tt < c.ntok; ++tt) {
-                        float acc = pbuf[(lane * nb) * NT + tt];
+                        float acc = pbuf[lane * prow + tt];
 #pragma unroll 4
-                        for (int bb = 1; bb < nb; ++bb) acc += pbuf[(lane * nb + bb) * NT + tt];
+                        for (int bb = 1; bb < nb; ++bb) acc += pbuf[lane * prow + bb * NT + tt];
                         c.y[(int64_t)tt * c.rows + g0 + lane] =
                             bad ? __int_as_float(0x7FC00000) : acc;
                     }

@@ -105,15 +105,16 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
         M.rows_r = (int)(m.rows % ncta[i]);
         cta += ncta[i];
         // rows per group: partials for the group must fit in 64 KiB
-        const int64_t part_row = (int64_t)nb * ntok_part * 4;
+        const int64_t part_row = (int64_t)kq::part_row_floats(nb, ntok_part) * 4;
         int rmax = (int)std::min<int64_t>(64 * 1024 / part_row, rcap);
         if (rmax < 1) return KQ_ERR_SHAPE;
         // Whole Q6_K rows (dp4a launches): a stage is one group of about
         // kb_bytes x rcap bytes of consecutive rows.  Taken when a CTA's
-        // rows fit in one such stage, or are more than one group of row
-        // segments anyway; in between, whole-row stages would split a
-        // single segment group into several (measured slower at 27 rows
-        // per CTA: 9.20 vs 8.44 us on Q6_K 4096x6656).  Tensor-core
+        // rows fit in one such stage, or make many groups of row segments
+        // anyway (eight or more: the LM head's 1329 rows per CTA); in
+        // between, whole-row stages split a few segment groups into more
+        // (measured slower at 27 rows per CTA on Q6_K 4096x6656: 9.20 vs
+        // 8.44 us at ntok 1, 19.05 vs 15.87 us at ntok 3).  Tensor-core
         // launches keep segments: their units read every stage's columns'
         // input fragments, which whole-row stages of few rows would
         // multiply.
@@ -121,7 +122,10 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
             const int hw = (int)std::max<int64_t>(
                 1, std::min<int64_t>(rmax, (int64_t)kb_bytes * rcap / M.row_bytes));
             const int64_t cta_rows = M.rows_q + (M.rows_r > 0 ? 1 : 0);
-            if (cta_rows <= hw || cta_rows > rmax) {
+            // ... and only in stages of 8 or more rows: the LM head at 3
+            // token columns (16-row groups, 6-row whole-row stages) took
+            // 547 us against 406 with row segments
+            if (hw >= 8 && (cta_rows <= hw || cta_rows >= 8 * (int64_t)rmax)) {
                 M.whole = 1;
                 rmax = hw;
             }
