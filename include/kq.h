@@ -245,7 +245,10 @@ kq_status kq_device_error(int clear);
 /*
  * Kernel selection, for testing and measurement: 0 = automatic (the
  * TMA-streaming kernel whenever the shapes can be staged in shared memory,
- * else the direct-load kernel), 1 = always the direct-load kernel, 2 = only
+ * else the direct-load kernel; with 9..16 token columns on the tensor
+ * cores, also the direct-load kernel where the streaming kernel's CTAs
+ * would hold several row groups that fill less than four fifths of their
+ * 16-row tiles), 1 = always the direct-load kernel, 2 = only
  * the streaming kernel (calls it cannot stage return KQ_ERR_SHAPE with
  * nothing enqueued).  Both kernels compute every output with the same
  * arithmetic in the same order, so results do not depend on this setting.

@@ -15,7 +15,7 @@ extern "C" {
 
 /* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
  * KQ_PLAN_MEMBER per member. */
-#define KQ_PLAN_HEAD 12
+#define KQ_PLAN_HEAD 13
 #define KQ_PLAN_MEMBER 21
 
 /*
@@ -34,7 +34,11 @@ extern "C" {
  *   [7] nslot  [8] dynamic shared memory  [9] stages of the largest CTA
  *   [10] bytes of the tensor-core units' scratch (0 for dp4a launches)
  *   [11] partial buffers (2; 1 for a tensor-core launch whose CTAs have
- *   one row group each)
+ *   one row group each)  [12] tensor-core launches: 1 if the library takes
+ *   the streaming kernel for this plan under automatic kernel selection,
+ *   0 if it takes the direct-load kernel (two octets of tokens and several
+ *   row groups a CTA that fill less than four fifths of their 16-row
+ *   tiles); 0 for dp4a launches and failed plans
  *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
  *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes, whole (Q6_K
  *   stages of whole rows, one bulk copy each: 1; else 0).

@@ -712,8 +712,12 @@ kq_status run_direct_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     return KQ_OK;
 }
 
+// The tensor-core streaming launch; with `automatic` (no kernel forced) it
+// declines plans where the direct-load kernel is expected to be faster
+// (kqplan::tc_stream_preferred), launching nothing.
 kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
-                        const DeviceInfo &info, const uint8_t *const *rec, bool *launched) {
+                        const DeviceInfo &info, const uint8_t *const *rec, bool automatic,
+                        bool *launched) {
     *launched = false;
     static kq::StreamParams p;  // ~10 KB: kept off the stack
     static std::mutex pmu;
@@ -724,6 +728,7 @@ kq_status run_stream_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     kqplan::Plan P;
     const kq_status ps = kqplan::plan_stream(mats, n, ntok, info.sms, info.smem_optin, &P, noct);
     if (ps != KQ_OK) return ps;
+    if (automatic && !kqplan::tc_stream_preferred(P)) return KQ_ERR_SHAPE;
     for (int i = 0; i < n; ++i) {
         const kq_mat &m = mats[i];
         const kqplan::Member &Q = P.m[i];
@@ -911,7 +916,7 @@ kq_status run_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s) {
     }
     kq_status st = KQ_ERR_SHAPE;
     bool launched = false;
-    if (choice != 1) st = run_stream_tc(mats, n, ntok, s, info, rec, &launched);
+    if (choice != 1) st = run_stream_tc(mats, n, ntok, s, info, rec, choice == 0, &launched);
     if (!launched && choice != 2) st = run_direct_tc(mats, n, ntok, s, info, rec);
     e = cudaFreeAsync(owned, s);
     if (st == KQ_OK && e != cudaSuccess) {

@@ -247,6 +247,7 @@ struct ConsumerCtx {
     float *part_f;
     int part_step;        // floats from partial buffer 0 to 1 (0: one buffer)
     float *scr;           // tensor-core unit scratch (consumer warp 0's; then per warp)
+    int scr_tiles;        // tiles of scales a warp's scratch holds (1 or 2)
     int ntok;
     uint32_t bars, ring, xbar;
     int nslot, slot_bytes;
@@ -441,9 +442,53 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
     reduce_last_group(c, NTOK, NTOK, warp, lane);
 }
 
+// One unit of a tensor-core launch: block column j of the stage (column
+// b0 + j of the rows) for rows r0.. of the group's h rows as MT 16-row
+// tiles, its partials stored in pbuf.  `base`: the Q6_K stage's first row
+// offset (see q6_row_off).
+template <int FMT, int NOCT, int MT>
+__device__ __forceinline__ void tc_column(const ConsumerCtx &c, const uint8_t *sdp, uint32_t base,
+                                          int b0, int j, int r0, int h, const uint8_t *col,
+                                          float *scr, float *pbuf, int lane) {
+    constexpr bool Q6 = FMT == kFmtQ6K;
+    constexpr int BB = Q6 ? 210 : (FMT == kFmtQ5K ? 176 : 144);
+    constexpr int NT = 8 * NOCT;
+    const int prow = part_row_floats(c.nb, NT);
+    const int nvalid = h - r0 < 16 * MT ? h - r0 : 16 * MT;
+    float v[MT][NOCT][2][2];
+    if (!Q6) {
+        const uint8_t *blk = sdp + r0 * (c.kb * BB) + j * BB;
+        const int rs = c.kb * BB;
+        tc_unit_mt<FMT, NOCT, false, true, MT>([&](int r) { return blk + r * rs; }, nvalid, col,
+                                               c.ntok, scr, lane, v);
+    } else {
+        const uint32_t rb = (uint32_t)c.row_bytes;
+        tc_unit_mt<FMT, NOCT, false, true, MT>(
+            [&](int r) {
+                return sdp + q6_row_off(base, r0 + r, rb, c.q6_seg, c.q6_whole) + j * 210;
+            },
+            nvalid, col, c.ntok, scr, lane, v);
+    }
+    const int gg = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const int row = r0 + 16 * m + gg + 8 * k2;
+            if (row < h) {
+#pragma unroll
+                for (int o = 0; o < NOCT; ++o)
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+                        pbuf[row * prow + (b0 + j) * NT + 8 * o + 2 * t4 + jj] = v[m][o][k2][jj];
+            }
+        }
+}
+
 // The consumer of a tensor-core launch (ntok >= kTcMinNtok, any format):
-// the stage's work is cut into units of one 16-row tile x one block column
-// (kq_tc.cuh, all NOCT octets of tokens at once), and the CTA's whole
+// the stage's work is cut into units of one block column of one 16-row
+// tile, or of both tiles of a 32-row group with two octets of tokens
+// (tc_unit_tiles; kq_tc.cuh, all NOCT octets at once), and the CTA's whole
 // sequence of units, stage after stage, is dealt round-robin: warp w takes
 // units w, w + kStreamConsumers, ...  Each warp still waits for every
 // stage's slot and arrives on its empty barrier once per stage (see
@@ -452,11 +497,10 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
 template <int NOCT, int FMT>
 __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int lane) {
     constexpr int NT = 8 * NOCT;
-    constexpr bool Q6 = FMT == kFmtQ6K;
-    constexpr int BB = Q6 ? 210 : (FMT == kFmtQ5K ? 176 : 144);
     const int nb = c.nb;
     const int prow = part_row_floats(nb, NT);
-    float *scr = c.scr + warp * (kTcScrBytes / 4);
+    constexpr int MT = tc_unit_tiles(NOCT);
+    float *scr = c.scr + warp * c.scr_tiles * (kTcScrBytes / 4);
     constexpr int colb = tc_col_bytes(NOCT);
     int next = warp;  // this warp's next unit, counted over the whole CTA
     int ubase = 0;    // units of the stages before this one
@@ -468,7 +512,9 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
         const int b0 = k * c.kb;
         const int kbv = nb - b0 < c.kb ? nb - b0 : c.kb;
         const int tiles = (h + 15) >> 4;  // 1 or 2
-        const int units = tiles * kbv;
+        // one unit spans both tiles (the scratch holds both tiles' scales)
+        const bool pair = MT == 2 && tiles == 2 && c.scr_tiles == 2;
+        const int units = (pair ? 1 : tiles) * kbv;
         const uint8_t *sdp = c.smem + (c.ring - c.bars) + slot * c.slot_bytes;
         float *pbuf = c.part_f + (g & 1) * c.part_step;
         bool ok = !*(volatile int *)c.abort_flag;
@@ -490,36 +536,14 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
         for (; next < ubase + units; next += kStreamConsumers) {
             if (!ok) continue;
             const int ul = next - ubase;
-            const int j = tiles == 2 ? ul >> 1 : ul;  // block column within the stage
-            const int r0 = tiles == 2 ? (ul & 1) * 16 : 0;
-            const int nvalid = h - r0 < 16 ? h - r0 : 16;
-            float v[NOCT][2][2];
+            // block column within the stage, first row of the unit
+            const int j = (!pair && tiles == 2) ? ul >> 1 : ul;
+            const int r0 = (!pair && tiles == 2) ? (ul & 1) * 16 : 0;
             const uint8_t *col = c.recs + (int64_t)(b0 + j) * colb;  // column b0 + j's records
-            if (!Q6) {
-                const uint8_t *blk = sdp + r0 * (c.kb * BB) + j * BB;
-                const int rs = c.kb * BB;
-                tc_unit<FMT, NOCT, false, true>([&](int r) { return blk + r * rs; }, nvalid, col,
-                                                c.ntok, scr, lane, v);
-            } else {
-                const uint32_t rb = (uint32_t)c.row_bytes;
-                tc_unit<FMT, NOCT, false, true>(
-                    [&](int r) {
-                        return sdp + q6_row_off(base, r0 + r, rb, c.q6_seg, c.q6_whole) + j * 210;
-                    },
-                    nvalid, col, c.ntok, scr, lane, v);
-            }
-            const int gg = lane >> 2, t4 = lane & 3;
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int row = r0 + gg + 8 * k2;
-                if (row < h) {
-#pragma unroll
-                    for (int o = 0; o < NOCT; ++o)
-#pragma unroll
-                        for (int jj = 0; jj < 2; ++jj)
-                            pbuf[row * prow + (b0 + j) * NT + 8 * o + 2 * t4 + jj] = v[o][k2][jj];
-                }
-            }
+            if (pair)
+                tc_column<FMT, NOCT, MT>(c, sdp, base, b0, j, 0, h, col, scr, pbuf, lane);
+            else
+                tc_column<FMT, NOCT, 1>(c, sdp, base, b0, j, r0, h, col, scr, pbuf, lane);
         }
         ubase += units;
         __syncwarp();
@@ -771,6 +795,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.part_f = reinterpret_cast<float *>(smem + (parts - bars));
     c.part_step = p.part_bufs == 2 ? p.part_bytes / 8 : 0;
     c.scr = reinterpret_cast<float *>(smem + (scrs - bars));
+    c.scr_tiles = p.scr_bytes >= kStreamConsumers * 2 * kTcScrBytes ? 2 : 1;
     c.ntok = p.ntok;
     c.bars = bars;
     c.ring = ring;

@@ -199,7 +199,14 @@ kq_status plan_level(const kq_mat *mats, int n, int ntok, const int *ncta, int l
     P.part_bytes = P.part_bufs * round_up(P.part_bytes, 128);
     P.slot_bytes = round_up(P.slot_bytes, 128);
     P.x_bytes = round_up(P.x_bytes, 128);
-    if (tc) P.scr_bytes = round_up((int64_t)kq::kStreamConsumers * kq::kTcScrBytes, 128);
+    // tensor-core launches: each consumer warp's unit scratch, two tiles'
+    // scales where units span two tiles (groups of more than 16 rows)
+    if (tc) {
+        int64_t hmax = 0;
+        for (int i = 0; i < n; ++i) hmax = std::max<int64_t>(hmax, P.m[i].hmax);
+        const int tiles = hmax > 16 ? kq::tc_unit_tiles(P.tc_noct) : 1;
+        P.scr_bytes = round_up((int64_t)kq::kStreamConsumers * tiles * kq::kTcScrBytes, 128);
+    }
     P.grid = cta;
     return KQ_OK;
 }
@@ -241,6 +248,25 @@ kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_opt
     return KQ_OK;
 }
 
+bool tc_stream_preferred(const Plan &P) {
+    if (P.tc_noct < 2) return true;
+    for (int i = 0; i < P.n; ++i) {
+        const Member &M = P.m[i];
+        // CTAs of rows_q rows exist when rows_r < ncta, of rows_q + 1 when rows_r > 0
+        const bool occurs[2] = {M.rows_r < M.ncta, M.rows_r > 0};
+        for (int big = 0; big < 2; ++big) {
+            if (!occurs[big] || M.ng[big] <= 1) continue;
+            // groups of gq rows, and of gq + 1 when gr > 0: each must fill
+            // four fifths of its 16-row tiles
+            for (int hh = M.gq[big]; hh <= M.gq[big] + (M.gr[big] > 0 ? 1 : 0); ++hh) {
+                const int tiles = (hh + 15) / 16;
+                if (5 * hh < 4 * 16 * tiles) return false;
+            }
+        }
+    }
+    return true;
+}
+
 }  // namespace kqplan
 
 extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
@@ -265,6 +291,7 @@ extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, in
     *o++ = P.stages;
     *o++ = P.scr_bytes;
     *o++ = P.part_bufs;
+    *o++ = st == KQ_OK && noct > 0 ? (kqplan::tc_stream_preferred(P) ? 1 : 0) : 0;
     for (int i = 0; i < n; ++i) {
         const kqplan::Member &M = P.m[i];
         const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],

@@ -53,6 +53,18 @@ constexpr int64_t kCostQ6 = 32;
 // columns (one buffer when no CTA has a second row group), and one unit
 // scratch per consumer warp.  KQ_ERR_SHAPE when no geometry fits (the
 // caller then uses the direct-load kernel).
+// Tensor-core launches with two octets of tokens (9..16 columns): whether
+// the streaming kernel is expected to beat the direct-load kernel on this
+// plan.  It is where each CTA's rows form one group, or where every group
+// fills at least four fifths of its 16-row tiles; with several thinner
+// groups a CTA (each summed by one warp while the others go on, with twice
+// the partials of one octet, and fewer weight slots beside them) the direct
+// kernel's full 16-row tiles were faster on GB300: 6656x6656 Q4_K 26.7 vs
+// 32.5 us, Q6_K 28.0 vs 39.0, FFN down 6656x19968 Q6_K 122.6 vs 150.5, while
+// 4096x6656, 3072x6656 (one group) and 8192x6656 Q5_K (groups of 26-27
+// rows) ran faster streamed.  One octet: always true.
+bool tc_stream_preferred(const Plan &P);
+
 kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out,
                       int tc_noct = 0);
 

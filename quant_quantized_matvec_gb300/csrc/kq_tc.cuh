@@ -47,6 +47,12 @@ namespace kq {
 // together falls on eight different banks.
 constexpr int kTcScrStride = 28;
 constexpr int kTcScrBytes = 16 * kTcScrStride * 4;
+// 16-row tiles of a streaming-kernel unit at most: with two octets of
+// tokens a unit's input fragments are twice the bytes, and a group's two
+// tiles (17..32 rows) share them; at one octet a unit is one tile (dealing
+// twice as many units evens out the warps' work).  A consumer warp's
+// scratch holds that many tiles' scales where the launch has such groups.
+__host__ __device__ constexpr int tc_unit_tiles(int noct) { return noct >= 2 ? 2 : 1; }
 
 // D += A * B over one 16 x 16 x 8 tile, f16 operands, f32 accumulators.
 // (A pure register operation: not volatile, so loads may be scheduled
@@ -159,16 +165,19 @@ __device__ __forceinline__ void tc_a_from_bytes(uint32_t wa, uint32_t wb, uint32
     a[3] = (wb >> 8) & mask;
 }
 
-// One unit.  Rows r of the tile at rowp(r) (r < nvalid), one block column,
-// NOCT octets of tokens; `col` = this column's input records (kq_xtc.cuh:
-// the fragments of octets 0..NOCT-1, then the aux of tokens 0..8 NOCT - 1),
-// in global memory (GB) or shared memory; `ntok` the launch's token
-// columns.  GW: the weights are in global memory.  Returns v[o][k2][j] for
-// row g + 8 k2 and token 8o + 2t + j in lane (g, t); tokens past ntok are
+// One unit: MT tiles of 16 rows (tile m = rows 16m..16m+15 at rowp(r); rows
+// past nvalid - 1 repeat row nvalid - 1), one block column, NOCT octets of
+// tokens; `col` = this column's input records (kq_xtc.cuh: the fragments of
+// octets 0..NOCT-1, then the aux of tokens 0..8 NOCT - 1), in global memory
+// (GB) or shared memory; `ntok` the launch's token columns.  GW: the weights
+// are in global memory.  The tiles share every B fragment load; each tile's
+// operations are those of a one-tile unit, in the same order.  `scr` holds
+// MT tiles' scales (MT x kTcScrBytes).  Returns v[m][o][k2][j] for row
+// 16m + g + 8 k2 and token 8o + 2t + j in lane (g, t); tokens past ntok are
 // garbage and not to be stored.
-template <int FMT, int NOCT, bool GW, bool GB, class RowP>
-__device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *col, int ntok,
-                                        float *scr, int lane, float (&v)[NOCT][2][2]) {
+template <int FMT, int NOCT, bool GW, bool GB, int MT, class RowP>
+__device__ __forceinline__ void tc_unit_mt(RowP rowp, int nvalid, const uint8_t *col, int ntok,
+                                           float *scr, int lane, float (&v)[MT][NOCT][2][2]) {
     const uint8_t *frag = col;
     constexpr int ostride = kTcFragOctBytes;
     const float *aux = reinterpret_cast<const float *>(col + NOCT * kTcFragOctBytes);
@@ -186,67 +195,98 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
         if constexpr (PRE) return bpre[k];
         return tc_ld<GB, uint4>(fo + tc_frag_offset(k, 0));
     };
-    tc_scales<FMT, GW>(rowp, nvalid, scr, lane);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+        tc_scales<FMT, GW>([&](int r) { return rowp(16 * m + r); }, nvalid - 16 * m,
+                           scr + 16 * m * kTcScrStride, lane);
     __syncwarp();
     const int g = lane >> 2, t = lane & 3;
-    const uint8_t *pa = rowp(g < nvalid ? g : nvalid - 1);
-    const uint8_t *pb = rowp(g + 8 < nvalid ? g + 8 : nvalid - 1);
-    const float *Fa = scr + g * kTcScrStride, *Fb = scr + (g + 8) * kTcScrStride;
-    float acc[NOCT][2][2];
+    const uint8_t *pa[MT], *pb[MT];
+    const float *Fa[MT], *Fb[MT];
 #pragma unroll
-    for (int o = 0; o < NOCT; ++o)
-        acc[o][0][0] = acc[o][0][1] = acc[o][1][0] = acc[o][1][1] = 0.0f;
+    for (int m = 0; m < MT; ++m) {
+        const int ra = 16 * m + g, rb = ra + 8;
+        pa[m] = rowp(ra < nvalid ? ra : nvalid - 1);
+        pb[m] = rowp(rb < nvalid ? rb : nvalid - 1);
+        Fa[m] = scr + ra * kTcScrStride;
+        Fb[m] = scr + rb * kTcScrStride;
+    }
+    float acc[MT][NOCT][2][2];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int o = 0; o < NOCT; ++o)
+            acc[m][o][0][0] = acc[m][o][0][1] = acc[m][o][1][0] = acc[m][o][1][1] = 0.0f;
     const uint8_t *fl = frag + lane * 16;
     if (FMT != kFmtQ6K) {
         constexpr bool Q5 = FMT == kFmtQ5K;
         constexpr int QS = Q5 ? 48 : 16;
         const uint32_t m4 = 0x000F000Fu, m5 = 0x001F001Fu;
-        uint32_t qha[2] = {0, 0}, qhb[2] = {0, 0};
-        if (Q5) {  // qh bytes 16 * half + 4t .. + 3 of the two rows
+        uint32_t qha[MT][2], qhb[MT][2];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                qha[hf] = tc_ld<GW, uint32_t>(pa + 16 + 16 * hf + 4 * t);
-                qhb[hf] = tc_ld<GW, uint32_t>(pb + 16 + 16 * hf + 4 * t);
+        for (int m = 0; m < MT; ++m) {
+            qha[m][0] = qha[m][1] = qhb[m][0] = qhb[m][1] = 0u;
+            if (Q5) {  // qh bytes 16 * half + 4t .. + 3 of the two rows
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    qha[m][hf] = tc_ld<GW, uint32_t>(pa[m] + 16 + 16 * hf + 4 * t);
+                    qhb[m][hf] = tc_ld<GW, uint32_t>(pb[m] + 16 + 16 * hf + 4 * t);
+                }
             }
         }
 #pragma unroll
         for (int gp = 0; gp < 4; ++gp) {
             // qs words of k-step halves 0 and 1 of group gp (sub-blocks 2gp, 2gp + 1)
-            uint32_t wa[2], wb[2];
+            uint32_t wa[MT][2], wb[MT][2];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                wa[hf] = tc_ld<GW, uint32_t>(pa + QS + 32 * gp + 16 * hf + 4 * t);
-                wb[hf] = tc_ld<GW, uint32_t>(pb + QS + 32 * gp + 16 * hf + 4 * t);
-            }
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    wa[m][hf] = tc_ld<GW, uint32_t>(pa[m] + QS + 32 * gp + 16 * hf + 4 * t);
+                    wb[m][hf] = tc_ld<GW, uint32_t>(pb[m] + QS + 32 * gp + 16 * hf + 4 * t);
+                }
 #pragma unroll
             for (int hi = 0; hi < 2; ++hi) {
                 const int s = 2 * gp + hi;
-                uint32_t A[2][4];
+                uint32_t A[MT][2][4];
+                float fa[MT], fb[MT];
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t ca = hi ? (wa[hf] >> 4) & 0x0F0F0F0Fu : wa[hf] & 0x0F0F0F0Fu;
-                    uint32_t cb = hi ? (wb[hf] >> 4) & 0x0F0F0F0Fu : wb[hf] & 0x0F0F0F0Fu;
-                    if (Q5) {  // bit s of each qh byte as bit 4 of the code
-                        ca |= (s <= 4 ? qha[hf] << (4 - s) : qha[hf] >> (s - 4)) & 0x10101010u;
-                        cb |= (s <= 4 ? qhb[hf] << (4 - s) : qhb[hf] >> (s - 4)) & 0x10101010u;
+                for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t ca = hi ? (wa[m][hf] >> 4) & 0x0F0F0F0Fu : wa[m][hf] & 0x0F0F0F0Fu;
+                        uint32_t cb = hi ? (wb[m][hf] >> 4) & 0x0F0F0F0Fu : wb[m][hf] & 0x0F0F0F0Fu;
+                        if (Q5) {  // bit s of each qh byte as bit 4 of the code
+                            ca |= (s <= 4 ? qha[m][hf] << (4 - s) : qha[m][hf] >> (s - 4)) & 0x10101010u;
+                            cb |= (s <= 4 ? qhb[m][hf] << (4 - s) : qhb[m][hf] >> (s - 4)) & 0x10101010u;
+                        }
+                        tc_a_from_bytes(ca, cb, Q5 ? m5 : m4, A[m][hf]);
                     }
-                    tc_a_from_bytes(ca, cb, Q5 ? m5 : m4, A[hf]);
+                    fa[m] = Fa[m][s];
+                    fb[m] = Fb[m][s];
                 }
-                const float fa = Fa[s], fb = Fb[s];
 #pragma unroll
                 for (int o = 0; o < NOCT; ++o) {
                     const uint8_t *fo = fl + o * ostride;
-                    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    float D[MT][4];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) D[m][0] = D[m][1] = D[m][2] = D[m][3] = 0.0f;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         const uint4 b = bfrag(fo, 2 * s + hf);
-                        mma_f16(D, A[hf], b.x, b.y);  // hi
-                        mma_f16(D, A[hf], b.z, b.w);  // lo
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            mma_f16(D[m], A[m][hf], b.x, b.y);  // hi
+                            mma_f16(D[m], A[m][hf], b.z, b.w);  // lo
+                        }
                     }
-                    acc[o][0][0] = fmaf(fa, D[0], acc[o][0][0]);
-                    acc[o][0][1] = fmaf(fa, D[1], acc[o][0][1]);
-                    acc[o][1][0] = fmaf(fb, D[2], acc[o][1][0]);
-                    acc[o][1][1] = fmaf(fb, D[3], acc[o][1][1]);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        acc[m][o][0][0] = fmaf(fa[m], D[m][0], acc[m][o][0][0]);
+                        acc[m][o][0][1] = fmaf(fa[m], D[m][1], acc[m][o][0][1]);
+                        acc[m][o][1][0] = fmaf(fb[m], D[m][2], acc[m][o][1][0]);
+                        acc[m][o][1][1] = fmaf(fb[m], D[m][3], acc[m][o][1][1]);
+                    }
                 }
             }
         }
@@ -263,17 +303,18 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
                 const float u = tc_ld<GB, float>(ax + kTcAuxU);
                 const float S[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const float *dm = (k2 ? Fb : Fa) + 16;
-                    float mt = dm[0] * S[0];
+                for (int m = 0; m < MT; ++m)
 #pragma unroll
-                    for (int s = 1; s < 8; ++s) mt = fmaf(dm[s], S[s], mt);
-                    v[o][k2][j] = u * (acc[o][k2][j] - mt);
-                }
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const float *dm = (k2 ? Fb[m] : Fa[m]) + 16;
+                        float mt = dm[0] * S[0];
+#pragma unroll
+                        for (int s = 1; s < 8; ++s) mt = fmaf(dm[s], S[s], mt);
+                        v[m][o][k2][j] = u * (acc[m][o][k2][j] - mt);
+                    }
             }
         }
     } else {
-        const Q6Row<GW> qa = Q6Row<GW>::at(pa), qb = Q6Row<GW>::at(pb);
         const uint32_t m6 = 0x003F003Fu;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -282,32 +323,49 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
                 // ql words (quadrant pairs 0/2 and 1/3) and the qh word of
                 // inputs 128h + 16kh + 4t .. (+32q) of the two rows
                 const int w0 = 16 * h + 4 * kh + t, w1 = w0 + 8, wq = 32 + 8 * h + 4 * kh + t;
-                const uint32_t la0 = qa.word(w0), la1 = qa.word(w1), lqa = qa.word(wq);
-                const uint32_t lb0 = qb.word(w0), lb1 = qb.word(w1), lqb = qb.word(wq);
+                uint32_t la0[MT], la1[MT], lqa[MT], lb0[MT], lb1[MT], lqb[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const Q6Row<GW> qa = Q6Row<GW>::at(pa[m]), qb = Q6Row<GW>::at(pb[m]);
+                    la0[m] = qa.word(w0);
+                    la1[m] = qa.word(w1);
+                    lqa[m] = qa.word(wq);
+                    lb0[m] = qb.word(w0);
+                    lb1[m] = qb.word(w1);
+                    lqb[m] = qb.word(wq);
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int s = 8 * h + 2 * q + kh;
-                    const uint32_t la = (q & 1) ? la1 : la0, lb = (q & 1) ? lb1 : lb0;
-                    const uint32_t ca = (q < 2 ? la & 0x0F0F0F0Fu : (la >> 4) & 0x0F0F0F0Fu) |
-                                        (((lqa >> (2 * q)) & 0x03030303u) << 4);
-                    const uint32_t cb = (q < 2 ? lb & 0x0F0F0F0Fu : (lb >> 4) & 0x0F0F0F0Fu) |
-                                        (((lqb >> (2 * q)) & 0x03030303u) << 4);
-                    uint32_t A[4];
-                    tc_a_from_bytes(ca, cb, m6, A);
+                    uint32_t A[MT][4];
+                    float fa[MT], fb[MT];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) A[i] = tc_minus32(A[i]);
-                    const float fa = Fa[s], fb = Fb[s];
+                    for (int m = 0; m < MT; ++m) {
+                        const uint32_t la = (q & 1) ? la1[m] : la0[m], lb = (q & 1) ? lb1[m] : lb0[m];
+                        const uint32_t ca = (q < 2 ? la & 0x0F0F0F0Fu : (la >> 4) & 0x0F0F0F0Fu) |
+                                            (((lqa[m] >> (2 * q)) & 0x03030303u) << 4);
+                        const uint32_t cb = (q < 2 ? lb & 0x0F0F0F0Fu : (lb >> 4) & 0x0F0F0F0Fu) |
+                                            (((lqb[m] >> (2 * q)) & 0x03030303u) << 4);
+                        tc_a_from_bytes(ca, cb, m6, A[m]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) A[m][i] = tc_minus32(A[m][i]);
+                        fa[m] = Fa[m][s];
+                        fb[m] = Fb[m][s];
+                    }
 #pragma unroll
                     for (int o = 0; o < NOCT; ++o) {
                         const uint8_t *fo = fl + o * ostride;
-                        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                         const uint4 b = bfrag(fo, s);
-                        mma_f16(D, A, b.x, b.y);  // hi
-                        mma_f16(D, A, b.z, b.w);  // lo
-                        acc[o][0][0] = fmaf(fa, D[0], acc[o][0][0]);
-                        acc[o][0][1] = fmaf(fa, D[1], acc[o][0][1]);
-                        acc[o][1][0] = fmaf(fb, D[2], acc[o][1][0]);
-                        acc[o][1][1] = fmaf(fb, D[3], acc[o][1][1]);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            mma_f16(D, A[m], b.x, b.y);  // hi
+                            mma_f16(D, A[m], b.z, b.w);  // lo
+                            acc[m][o][0][0] = fmaf(fa[m], D[0], acc[m][o][0][0]);
+                            acc[m][o][0][1] = fmaf(fa[m], D[1], acc[m][o][0][1]);
+                            acc[m][o][1][0] = fmaf(fb[m], D[2], acc[m][o][1][0]);
+                            acc[m][o][1][1] = fmaf(fb[m], D[3], acc[m][o][1][1]);
+                        }
                     }
                 }
             }
@@ -319,12 +377,23 @@ __device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *co
                 int tok = 8 * o + 2 * t + j;
                 tok = tok < ntok ? tok : ntok - 1;
                 const float u = tc_ld<GB, float>(aux + tok * taux + kTcAuxU);
-                v[o][0][j] = u * acc[o][0][j];
-                v[o][1][j] = u * acc[o][1][j];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    v[m][o][0][j] = u * acc[m][o][0][j];
+                    v[m][o][1][j] = u * acc[m][o][1][j];
+                }
             }
         }
     }
     __syncwarp();  // the scratch is free for the next unit
+}
+
+// One tile of 16 rows (tc_unit_mt with MT = 1): v[o][k2][j] for row g + 8 k2.
+template <int FMT, int NOCT, bool GW, bool GB, class RowP>
+__device__ __forceinline__ void tc_unit(RowP rowp, int nvalid, const uint8_t *col, int ntok,
+                                        float *scr, int lane, float (&v)[NOCT][2][2]) {
+    tc_unit_mt<FMT, NOCT, GW, GB, 1>(rowp, nvalid, col, ntok, scr, lane,
+                                     *reinterpret_cast<float (*)[1][NOCT][2][2]>(&v));
 }
 
 }  // namespace kq

@@ -173,3 +173,32 @@ def test_set_mixing_arithmetics_equals_separate_calls():
         assert np.array_equal(bits(gs.host()), bits(gp.host()))
         C.check(fmt, W, rows, cols, x, gs.host(), what="mixed set ntok=3")
     assert not kq.device_error()
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=NAMES.get)
+@pytest.mark.parametrize("rows", [152 * 17, 152 * 27 + 5, 152 * 32, 152 * 45 + 7])
+@pytest.mark.parametrize("ntok", [9, 16])
+def test_two_tile_units_equal_the_direct_kernel(fmt, rows, ntok):
+    """With two octets of tokens the streaming kernel's units span both
+    16-row tiles of a group of 17..32 rows and share each fragment load
+    (groups of 17, 27-28, 32 and 22-23 rows here, some CTAs one row more):
+    every output equals the direct-load kernel's (16-row CTAs, one tile a
+    unit) bit for bit, and the oracle's within the tolerance."""
+    cols = 2816
+    W, x = C.case(fmt, rows, cols, ntok, f"n16/tiles/{fmt}/{rows}/{ntok}")
+    Wd, xd = C.to_dev(W), C.to_dev(x)
+    outs = {}
+    try:
+        for kernel in ("stream", "direct"):
+            kq.select_kernel(kernel)
+            g = C.Guarded(ntok, rows)
+            kq.matvec(fmt, Wd, rows, cols, xd, y=g.y)
+            torch.cuda.synchronize()
+            lk = kq.last_kernels()
+            assert lk["tensor_cores"] and lk[kernel]
+            outs[kernel] = g.host()
+    finally:
+        kq.select_kernel("auto")
+    assert np.array_equal(bits(outs["stream"]), bits(outs["direct"]))
+    C.check(fmt, W, rows, cols, x, outs["stream"], what=f"{NAMES[fmt]} {rows} rows ntok={ntok}")
+    assert not kq.device_error()

@@ -11,9 +11,10 @@ import pytest
 
 from quant_quantized_matvec_gb300 import _binding
 
-HEAD, MEMBER = 12, 21
+HEAD, MEMBER = 13, 21
 TC_MIN = 4                      # ntok from which the tensor-core path runs
-TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps
+TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps, one 16-row tile
+# ... and two tiles where units span both tiles of a group (ntok 9..16, groups of 17+ rows)
 SMS, SMEM = 152, 232448          # GB300: SMs, opt-in shared memory per CTA
 BB = {12: 144, 13: 176, 14: 210}
 REC = {12: 832, 13: 832, 14: 1056}
@@ -30,7 +31,8 @@ def plan(members, ntok, sms=SMS, smem=SMEM):
     assert lib.kq_plan_describe(arr, len(members), ntok, sms, smem, out, len(out)) == 0
     o = list(out)
     head = dict(zip(["status", "grid", "level", "xsmem", "x_bytes", "part_bytes",
-                     "slot_bytes", "nslot", "smem", "stages", "scr_bytes", "part_bufs"],
+                     "slot_bytes", "nslot", "smem", "stages", "scr_bytes", "part_bufs",
+                     "tc_stream"],
                     o[:HEAD]))
     keys = ["ncta", "cta_begin", "rows_q", "rows_r", "ng0", "gq0", "gr0", "ng1", "gq1",
             "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes",
@@ -111,12 +113,29 @@ def check(members, ntok, sms=SMS, smem=SMEM):
                          + h["nslot"] * h["slot_bytes"])
     # tensor-core launches: records in global memory, the units' scratch
     if ntok >= TC_MIN:
-        assert not h["xsmem"] and h["scr_bytes"] >= TC_SCR
+        tall = max(m["hmax"] for m in mem) > 16  # units of two tiles
+        assert not h["xsmem"] and h["scr_bytes"] == TC_SCR * (2 if ntok > 8 and tall else 1)
     else:
         assert h["scr_bytes"] == 0
     assert h["smem"] <= smem - 1024
     if not h["xsmem"]:
         assert h["x_bytes"] == 0 and h["level"] == -1
+    # routing under automatic kernel selection: one octet of tokens always
+    # streams; with two, several row groups a CTA must each fill 4/5 of
+    # their 16-row tiles
+    if ntok < TC_MIN:
+        assert h["tc_stream"] == 0
+    elif ntok <= 8:
+        assert h["tc_stream"] == 1
+    else:
+        fills = []
+        for m in mem:
+            occurs = [m["rows_r"] < m["ncta"], m["rows_r"] > 0]
+            for big in (0, 1):
+                if occurs[big] and m[f"ng{big}"] > 1:
+                    q, r = m[f"gq{big}"], m[f"gr{big}"]
+                    fills += [hh / (16 * -(-hh // 16)) for hh in ([q, q + 1] if r else [q])]
+        assert h["tc_stream"] == int(all(f >= 0.8 for f in fills))
     return h, mem
 
 
@@ -154,6 +173,24 @@ def test_random_sets():
     # the rest fall back to the direct kernel: mostly wide matrices at
     # 9..16 tensor-core columns, whose partials leave no room for two slots
     assert planned > 150
+
+
+@pytest.mark.parametrize("fmt,rows,cols,ntok,stream", [
+    (12, 4096, 6656, 16, 1),   # one 26-27 row group a CTA
+    (12, 3072, 6656, 16, 1),   # one 20-21 row group
+    (13, 8192, 6656, 16, 1),   # groups of 26-27 rows: 4/5 of two tiles
+    (12, 6656, 6656, 16, 0),   # groups of 21-22 rows
+    (12, 6656, 4096, 12, 0),
+    (14, 6656, 19968, 16, 0),  # groups of 10-11 rows
+    (12, 5120, 6656, 16, 0),   # groups of 16 and 17 rows
+    (12, 6656, 6656, 8, 1),    # one octet
+])
+def test_two_octet_launches_pick_the_kernel_measured_faster(fmt, rows, cols, ntok, stream):
+    """Which kernel the library takes for a tensor-core launch it can
+    stream (kq_plan.h, tc_stream_preferred: the streaming and direct-load
+    kernels timed on GB300 for each of these shapes)."""
+    h, _ = check([(fmt, rows, cols)], ntok)
+    assert h["status"] == OK and h["tc_stream"] == stream
 
 
 def test_more_members_than_sms_and_small_devices():
