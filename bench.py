@@ -360,12 +360,18 @@ def run_ours(args, rank, world, dist):
                for i, (f, r, c, p) in enumerate(members)]
         sets.append((mem, kq.make_set(mem)))
 
+    # the calls take their temporaries (tensor-core input fragments, staged
+    # host inputs, global input records) from one preallocated workspace
+    # (kq_matvec_set_ws) instead of stream-ordered allocations, so a step is
+    # kernels only; calls on one stream may share it
+    ws = torch.empty(max(kq.workspace_bytes(d, ntok) for _, d in sets),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
 
     def step(i):
         mem, d = sets[i % len(sets)]
-        kq.matvec_set(mem, ntok=ntok, stream=stream, descriptors=d)
+        kq.matvec_set(mem, ntok=ntok, stream=stream, descriptors=d, workspace=ws)
 
     K = args.steps
     L = min(K, args.graph_len)
@@ -489,7 +495,7 @@ def run_ours(args, rank, world, dist):
         def one(i):
             if host_y:
                 mem, d = host_sets[i % len(host_sets)]
-                kq.matvec_set(mem, ntok=ntok, stream=stream, descriptors=d)
+                kq.matvec_set(mem, ntok=ntok, stream=stream, descriptors=d, workspace=ws)
             else:
                 for p in xd:
                     xd[p].copy_(x_host[p], non_blocking=True)
@@ -549,6 +555,7 @@ def run_ours(args, rank, world, dist):
             "matrices": [f"{synth.FMT_NAMES[f]} {r}x{c}"
                          for f, r, c, _ in members],
             "bytes_per_step": step_bytes,
+            "workspace_bytes": int(ws.numel()),
             "l2": (f"inputs rotate over {copies} weight copies "
                    f"({copies * w_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)"
                    if copies > 1 else

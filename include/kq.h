@@ -44,7 +44,8 @@
  *     cudaFreeAsync on `stream`): the input records of calls whose records
  *     do not fit in shared memory, the fragments of the tensor-core
  *     arithmetic (8704 bytes per 256 inputs per group of 8 columns), and
- *     staged host inputs; kq_matvec_noalloc allocates nothing.
+ *     staged host inputs; kq_matvec_set_ws takes them from a caller's
+ *     workspace instead, and kq_matvec_noalloc allocates nothing.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream) and may be captured in a CUDA graph.
  *   - Every argument is validated on the host before anything is launched;
@@ -111,7 +112,8 @@ typedef enum kq_status {
     KQ_ERR_TIMEOUT = 8, /* a bounded device-side wait expired                 */
     /* codes beyond the eight of the problem statement's boundary:          */
     KQ_ERR_COUNT = 9,   /* set size outside 1..KQ_MAX_SET                     */
-    KQ_ERR_LIMIT = 10,  /* kq_matvec_noalloc: inputs beyond its fixed buffer  */
+    KQ_ERR_LIMIT = 10,  /* a fixed buffer too small: kq_matvec_noalloc's, or a
+                           kq_matvec_set_ws workspace                         */
     KQ_ERR_MEMORY = 11  /* W not in this device's memory, or x / y in memory
                            the device cannot address (pageable host memory,
                            another device's memory)                        */
@@ -195,6 +197,44 @@ typedef struct kq_mat {
  * Returns as kq_matvec; on error nothing is enqueued for any member.
  */
 kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream);
+
+/*
+ * Device workspace bytes that kq_matvec_set_ws needs for this set and ntok:
+ * room for every member's x as if it were staged, the tensor-core
+ * fragments of the members computed on the tensor cores, and the dp4a input
+ * records of the largest token chunk.  An upper bound of what the call
+ * uses, from the shapes and formats alone (no pointer is read or queried;
+ * no GPU is touched).  A negative kq_status for a set kq_matvec_set would
+ * reject on its arguments alone.
+ */
+int64_t kq_workspace_bytes(const kq_mat *mats, int n, int ntok);
+
+/*
+ * kq_matvec_set with a caller-provided device workspace instead of the
+ * library's stream-ordered temporaries: the call allocates nothing, so the
+ * work it enqueues is kernels only.  In a CUDA graph, or a stream with
+ * launch overlap on (kq_set_overlap), each call's input pass (the tensor-
+ * core fragments, the staging of host inputs) then overlaps the kernel
+ * before it, where an allocation between the kernels would have made it
+ * wait for that kernel to finish and launch afterwards.
+ *
+ *   ws        device (or managed) memory of the current device, 256-byte
+ *             aligned, not overlapping any member's W, x or y.  Owned by the
+ *             caller; the call's work on `stream` uses it until it has
+ *             finished, so calls that may run at the same time (different
+ *             streams, or graphs replayed concurrently) need separate
+ *             workspaces.  Its contents need not be initialised and are
+ *             garbage afterwards.
+ *   ws_bytes  at least kq_workspace_bytes(mats, n, ntok).
+ *
+ * Results are bitwise those of kq_matvec_set.  Errors as kq_matvec_set,
+ * plus, with nothing enqueued: KQ_ERR_LIMIT (ws_bytes too small),
+ * KQ_ERR_NULL (ws NULL), KQ_ERR_ALIGN (ws not 256-byte aligned),
+ * KQ_ERR_ALIAS (ws overlaps a member's buffers), KQ_ERR_MEMORY (ws not
+ * this device's memory).
+ */
+kq_status kq_matvec_set_ws(const kq_mat *mats, int n, int ntok, void *stream, void *ws,
+                           int64_t ws_bytes);
 
 /*
  * Rows of a K-quant matrix gathered by index and dequantized to f32 -- the

@@ -135,10 +135,26 @@ def make_set(members):
     return arr
 
 
-def matvec_set(members, ntok=None, stream=None, descriptors=None):
+def workspace_bytes(members, ntok):
+    """Bytes of the device workspace matvec_set(..., workspace=) needs for
+    these members (fmt, W, rows, cols, x, y) -- or descriptors from
+    make_set -- at ntok token columns (kq_workspace_bytes)."""
+    desc = members if isinstance(members, ctypes.Array) else make_set(members)
+    n = _lib().kq_workspace_bytes(ctypes.cast(desc, ctypes.POINTER(_binding.KqMat)),
+                                  len(desc), int(ntok))
+    if n < 0:
+        raise KQError(int(n), "kq_workspace_bytes")
+    return int(n)
+
+
+def matvec_set(members, ntok=None, stream=None, descriptors=None, workspace=None):
     """Several matvecs in one launch.  members: list of (fmt, W, rows, cols,
     x, y); x [ntok, cols] f32 (members may share x), y [ntok, rows] f32.
-    `descriptors` (from make_set) skips rebuilding the descriptor array."""
+    `descriptors` (from make_set) skips rebuilding the descriptor array.
+    `workspace`: a CUDA uint8 tensor of at least workspace_bytes(...) bytes,
+    256-byte aligned, taken instead of the library's stream-ordered
+    temporaries (kq_matvec_set_ws); it must not be used by another call
+    that may run at the same time."""
     import torch
     members = list(members)
     if ntok is None:
@@ -154,11 +170,17 @@ def matvec_set(members, ntok=None, stream=None, descriptors=None):
             if W.numel() * W.element_size() != matrix_bytes(fmt, rows, cols):
                 raise ValueError("W size does not match fmt/rows/cols")
         descriptors = make_set(members)
-    st = _lib().kq_matvec_set(
-        ctypes.cast(descriptors, ctypes.POINTER(_binding.KqMat)),
-        len(members), int(ntok), _stream_ptr(stream))
-    if st != 0:
-        raise KQError(st, "kq_matvec_set")
+    dp = ctypes.cast(descriptors, ctypes.POINTER(_binding.KqMat))
+    if workspace is None:
+        st = _lib().kq_matvec_set(dp, len(members), int(ntok), _stream_ptr(stream))
+        if st != 0:
+            raise KQError(st, "kq_matvec_set")
+    else:
+        st = _lib().kq_matvec_set_ws(dp, len(members), int(ntok), _stream_ptr(stream),
+                                     workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size())
+        if st != 0:
+            raise KQError(st, "kq_matvec_set_ws")
     return [m[5] for m in members]
 
 

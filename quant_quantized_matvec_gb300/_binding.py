@@ -18,7 +18,8 @@ STATUS = {
     10: "KQ_ERR_LIMIT", 11: "KQ_ERR_MEMORY",
 }
 SYMBOLS = ("kq_block_bytes", "kq_matrix_bytes", "kq_matvec",
-           "kq_matvec_set", "kq_status_str", "kq_last_cuda_error",
+           "kq_matvec_set", "kq_workspace_bytes", "kq_matvec_set_ws",
+           "kq_status_str", "kq_last_cuda_error",
            "kq_device_error", "kq_select_kernel", "kq_set_overlap",
            "kq_last_kernels", "kq_last_launch_count", "kq_matvec_noalloc", "kq_dequant_rows",
            "kq_version")
@@ -71,6 +72,10 @@ def load(path: str | None = None):
         lib.kq_matvec_noalloc.restype = i32
         lib.kq_matvec_set.argtypes = [ctypes.POINTER(KqMat), i32, i32, vp]
         lib.kq_matvec_set.restype = i32
+        lib.kq_workspace_bytes.argtypes = [ctypes.POINTER(KqMat), i32, i32]
+        lib.kq_workspace_bytes.restype = i64
+        lib.kq_matvec_set_ws.argtypes = [ctypes.POINTER(KqMat), i32, i32, vp, vp, i64]
+        lib.kq_matvec_set_ws.restype = i32
         lib.kq_status_str.argtypes = [i32]
         lib.kq_status_str.restype = ctypes.c_char_p
         lib.kq_last_cuda_error.argtypes = []

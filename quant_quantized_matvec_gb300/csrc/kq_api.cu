@@ -125,8 +125,12 @@ __global__ void __launch_bounds__(kTcPrepThreads) kq_xprep_tc(const __grid_const
     // before reading x (a no-op otherwise)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ uint32_t smax[kTcPrepSplit * 8];
+    static_assert(kTcPrepThreads == 32 * kTcPrepSplit, "one block per (plane, octet, column)");
+    // every plane's warps start at a multiple of kTcPrepSplit, so a block's
+    // warps all work or all return (build_tc_record holds a block barrier)
     const int64_t w = ((int64_t)blockIdx.x * kTcPrepThreads + threadIdx.x) >> 5;
-    if (w >= p.first_warp[p.n]) return;
+    if ((int64_t)blockIdx.x * kTcPrepSplit >= p.first_warp[p.n]) return;
     int k = 0;
 #pragma unroll 1
     for (int i = 1; i < p.n; ++i)
@@ -138,7 +142,8 @@ __global__ void __launch_bounds__(kTcPrepThreads) kq_xprep_tc(const __grid_const
     const int o = oj / nb, j = oj - o * nb;
     uint8_t *col = p.rec[k] + (int64_t)j * tc_col_bytes(noct);
     build_tc_record(p.x[k], p.ntok, nb, o, j, q, col + o * kTcFragOctBytes,
-                    reinterpret_cast<float *>(col + noct * kTcFragOctBytes), threadIdx.x & 31);
+                    reinterpret_cast<float *>(col + noct * kTcFragOctBytes), threadIdx.x & 31,
+                    smax);
 }
 
 }  // namespace kq
@@ -309,8 +314,43 @@ constexpr int kSmemLimit = kqlaunch::kDirectSmemLimit;
 // not build them in shared memory: one stream-ordered allocation, written
 // by kq_xprep and released (in stream order) after the kernel that reads
 // them.
+// ------------------------------------------------------------ workspace
+// The caller's device workspace of one kq_matvec_set_ws call: the call's
+// temporaries are carved from it instead of allocated.  Regions, in the
+// order the call takes them: staged host inputs, tensor-core fragments,
+// then the dp4a input records, whose region each token chunk reuses (a
+// chunk's record pass is an ordinary launch, so it starts only after the
+// kernel before it -- the previous chunk's matvec -- has finished).
+struct Arena {
+    uint8_t *base = nullptr;
+    int64_t size = 0, used = 0, chunk_mark = 0;
+};
+thread_local Arena *g_arena = nullptr;
+
+int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+
+// `bytes` of device memory for the current call: from the caller's
+// workspace when one is active (*owned = false), else a stream-ordered
+// temporary (*owned = true; the caller frees it on `s`).
+cudaError_t call_alloc(void **p, int64_t bytes, cudaStream_t s, bool *owned) {
+    *owned = false;
+    if (g_arena) {
+        const int64_t b = round256(bytes);
+        // kq_matvec_set_ws checked the size against kq_workspace_bytes, an
+        // upper bound of what a call takes: this does not fail
+        if (g_arena->used + b > g_arena->size) return cudaErrorMemoryAllocation;
+        *p = g_arena->base + g_arena->used;
+        g_arena->used += b;
+        return cudaSuccess;
+    }
+    const cudaError_t e = cudaMallocAsync(p, (size_t)bytes, s);
+    *owned = e == cudaSuccess;
+    return e;
+}
+
 struct GlobalRecords {
     uint8_t *buf = nullptr;
+    bool owned = false;  // a stream-ordered temporary (else the workspace's)
     const uint8_t *rec[KQ_MAX_SET] = {};
 };
 
@@ -332,7 +372,7 @@ cudaError_t prepare_records(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         warps += (int64_t)ntok * nb * 2;
     }
     p.first_warp[n] = warps;
-    cudaError_t e = cudaMallocAsync((void **)&out.buf, (size_t)total, s);
+    cudaError_t e = call_alloc((void **)&out.buf, total, s, &out.owned);
     if (e != cudaSuccess) return e;
     for (int i = 0; i < n; ++i) {
         p.rec[i] = out.buf + off[i];
@@ -342,7 +382,7 @@ cudaError_t prepare_records(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     kq::kq_xprep<<<(unsigned)blocks, kq::kPrepThreads, 0, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
-        cudaFreeAsync(out.buf, s);
+        if (out.owned) cudaFreeAsync(out.buf, s);
         out.buf = nullptr;
     }
     return e;
@@ -384,7 +424,7 @@ kq_status run_direct(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     if (e == cudaSuccess) {
         for (int i = 0; i < n; ++i) p.m[i].rec = gr.rec[i];
         e = kqlaunch::direct(ntok, p, (int)grid, smem, s);
-        const cudaError_t ef = cudaFreeAsync(gr.buf, s);
+        const cudaError_t ef = gr.owned ? cudaFreeAsync(gr.buf, s) : cudaSuccess;
         if (e == cudaSuccess) e = ef;
     }
     if (e != cudaSuccess) {
@@ -551,7 +591,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     }
     if (e == cudaSuccess) {
         e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s);
-        if (gr.buf) {
+        if (gr.owned) {
             const cudaError_t ef = cudaFreeAsync(gr.buf, s);
             if (e == cudaSuccess) e = ef;
         }
@@ -615,9 +655,10 @@ cudaError_t prepare_tc_records(const kq_mat *mats, int n, int ntok, cudaStream_t
     *owned = nullptr;
     const int64_t total = tc_records_bytes(mats, n, ntok);
     if (!buf) {
-        const cudaError_t e = cudaMallocAsync((void **)&buf, (size_t)total, s);
+        bool own = false;
+        const cudaError_t e = call_alloc((void **)&buf, total, s, &own);
         if (e != cudaSuccess) return e;
-        *owned = buf;
+        if (own) *owned = buf;
     }
     kq::TcPrepParams p{};
     p.ntok = ntok;
@@ -847,8 +888,9 @@ kq_status run_chunk(const kq_mat *mats, int n, int ntok, void *stream, bool afte
 // the members read it there instead of across the host link from every CTA.
 // *buf is the temporary (nullptr: nothing to stage).
 cudaError_t stage_inputs(kq_mat *mats, int n, int ntok, const bool *x_host, cudaStream_t s,
-                         void **buf) {
+                         void **buf, bool *owned) {
     *buf = nullptr;
+    *owned = false;
     kq::StageParams p{};
     const float *planes[KQ_MAX_SET];
     int64_t off[KQ_MAX_SET], total = 0;
@@ -869,7 +911,7 @@ cudaError_t stage_inputs(kq_mat *mats, int n, int ntok, const bool *x_host, cuda
         ++p.n;
     }
     if (p.n == 0) return cudaSuccess;
-    cudaError_t e = cudaMallocAsync(buf, (size_t)total, s);
+    cudaError_t e = call_alloc(buf, total, s, owned);
     if (e != cudaSuccess) {
         *buf = nullptr;
         return e;
@@ -918,7 +960,7 @@ kq_status run_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s) {
     bool launched = false;
     if (choice != 1) st = run_stream_tc(mats, n, ntok, s, info, rec, choice == 0, &launched);
     if (!launched && choice != 2) st = run_direct_tc(mats, n, ntok, s, info, rec);
-    e = cudaFreeAsync(owned, s);
+    e = owned ? cudaFreeAsync(owned, s) : cudaSuccess;
     if (st == KQ_OK && e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         st = KQ_ERR_CUDA;
@@ -941,9 +983,10 @@ kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
     if (r != KQ_OK) return r;
     cudaStream_t s = (cudaStream_t)stream;
     void *staged = nullptr;
-    cudaError_t se = stage_inputs(mats, n, ntok, x_host, s, &staged);
+    bool staged_owned = false;
+    cudaError_t se = stage_inputs(mats, n, ntok, x_host, s, &staged, &staged_owned);
     if (se != cudaSuccess) {
-        if (staged) cudaFreeAsync(staged, s);
+        if (staged_owned) cudaFreeAsync(staged, s);
         g_last_cuda_error = (int)se;
         return KQ_ERR_CUDA;
     }
@@ -960,6 +1003,7 @@ kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
         kernels = g_last_kernels;
         launches += g_last_launches;
     }
+    if (g_arena) g_arena->chunk_mark = g_arena->used;
     const int cn = launch_ntok();
     // dp4a: near-equal chunks, the first `rem` taking one column more
     const int nch = ndp > 0 ? (ntok + cn - 1) / cn : 0;
@@ -967,13 +1011,14 @@ kq_status run_set(const kq_mat *in, int n, int ntok, void *stream) {
     kq_mat part[KQ_MAX_SET];
     for (int ci = 0, t0 = 0; ci < nch && st == KQ_OK; ++ci) {
         const int nt = base + (ci < rem ? 1 : 0);
+        if (g_arena) g_arena->used = g_arena->chunk_mark;  // the chunks share one region
         token_chunk(dpm, ndp, t0, part);
         t0 += nt;
         st = run_chunk(part, ndp, nt, stream, after);
         kernels |= g_last_kernels;
         launches += g_last_launches;
     }
-    if (staged) {
+    if (staged_owned) {
         se = cudaFreeAsync(staged, s);
         if (st == KQ_OK && se != cudaSuccess) {
             g_last_cuda_error = (int)se;
@@ -1174,6 +1219,64 @@ kq_status kq_matvec_set(const kq_mat *mats, int n, int ntok, void *stream) {
     return run_set(mats, n, ntok, stream);
 }
 
+namespace {
+// An upper bound of what run_set takes from a workspace: every member's x
+// as if it were staged, the tensor-core members' fragments, and the dp4a
+// members' input records for the largest token chunk.
+int64_t workspace_need(const kq_mat *mats, int n, int ntok) {
+    int64_t stage = 0, dp = 0;
+    kq_mat tcm[KQ_MAX_SET];
+    int ntc = 0;
+    const int nt_chunk = std::min(ntok, kLaunchNtok);
+    for (int i = 0; i < n; ++i) {
+        const kq_mat &m = mats[i];
+        stage += round256((int64_t)ntok * m.cols * (int64_t)sizeof(float));
+        if (member_tc(m, ntok))
+            tcm[ntc++] = m;
+        else
+            dp += round256((int64_t)nt_chunk * (m.cols / 256) * kq::rec_bytes(m.fmt == KQ_Q6_K));
+    }
+    return stage + (ntc ? tc_records_bytes(tcm, ntc, ntok) : 0) + dp;
+}
+}  // namespace
+
+int64_t kq_workspace_bytes(const kq_mat *mats, int n, int ntok) {
+    const kq_status v = validate_set(mats, n, ntok);
+    if (v != KQ_OK) return -(int64_t)v;
+    return workspace_need(mats, n, ntok);
+}
+
+kq_status kq_matvec_set_ws(const kq_mat *mats, int n, int ntok, void *stream, void *ws,
+                           int64_t ws_bytes) {
+    const kq_status v = validate_set(mats, n, ntok);
+    if (v != KQ_OK) return v;
+    if (ws_bytes < workspace_need(mats, n, ntok)) return KQ_ERR_LIMIT;
+    if (!ws) return KQ_ERR_NULL;
+    if ((uintptr_t)ws & 255u) return KQ_ERR_ALIGN;
+    const Range rws{(uintptr_t)ws, (uintptr_t)ws + (uintptr_t)ws_bytes};
+    for (int i = 0; i < n; ++i)
+        if (overlaps(rws, w_range(mats[i])) || overlaps(rws, x_range(mats[i], ntok)) ||
+            overlaps(rws, y_range(mats[i], ntok)))
+            return KQ_ERR_ALIAS;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KQ_ERR_CUDA;
+    }
+    const void *alias = nullptr;
+    bool host = false;
+    const kq_status wst = device_address(ws, dev, false, &alias, &host);
+    if (wst != KQ_OK) return wst;
+    Arena a;
+    a.base = static_cast<uint8_t *>(ws);
+    a.size = ws_bytes;
+    g_arena = &a;
+    const kq_status st = run_set(mats, n, ntok, stream);
+    g_arena = nullptr;
+    return st;
+}
+
 kq_status kq_dequant_rows(int fmt, const void *W, int64_t rows, int64_t cols,
                           const int32_t *ids, int64_t n, float *out, void *stream) {
     const int64_t bb = block_bytes_of(fmt);
@@ -1239,7 +1342,7 @@ const char *kq_status_str(int status) {
     case KQ_ERR_COUNT: return "set size outside 1..16";
     case KQ_ERR_CUDA: return "a CUDA call failed (see kq_last_cuda_error)";
     case KQ_ERR_TIMEOUT: return "device-side wait timed out";
-    case KQ_ERR_LIMIT: return "inputs exceed the fixed buffer of kq_matvec_noalloc";
+    case KQ_ERR_LIMIT: return "a fixed buffer is too small (kq_matvec_noalloc's, or a kq_matvec_set_ws workspace)";
     case KQ_ERR_MEMORY: return "a pointer addresses memory the device cannot use there";
     default: return "unknown status";
     }
@@ -1280,7 +1383,7 @@ int kq_set_overlap(int enable) {
     return prev;
 }
 
-int kq_version(void) { return (1 << 16) | 3; }
+int kq_version(void) { return (1 << 16) | 4; }
 
 unsigned long long kq_set_wait_limit_ns(unsigned long long ns) {
     return g_wait_ns.exchange(ns);

@@ -64,33 +64,41 @@ __device__ __forceinline__ uint32_t half2_bits(__half a, __half b) {
     return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
 }
 
-// The records of one octet o and one column j, k-steps 4q..4q+3 (q = 0..3:
-// four warps share a column; each takes the column's maximum itself), built
-// by one warp.  x is [ntok][nb * 256]; `frag` points at this (octet,
-// column)'s fragments and `aux` at the column's aux of token 0.
+// The records of one octet o and one column j, k-steps 4q..4q+3, built by
+// warp q (0..3) of a block of four: each warp loads only its quarter of the
+// column (64 inputs of each of 8 tokens), the column's maximum per token is
+// taken over the four quarters' maxima in shared memory (smax, [4][8]
+// words).  x is [ntok][nb * 256]; `frag` points at this (octet, column)'s
+// fragments and `aux` at the column's aux of token 0.  Every thread of the
+// block calls this (it holds one block barrier).
 constexpr int kTcPrepSplit = 4;
 
 __device__ __forceinline__ void build_tc_record(const float *x, int ntok, int nb, int o, int j,
-                                                int q, uint8_t *frag, float *aux, int lane) {
+                                                int q, uint8_t *frag, float *aux, int lane,
+                                                uint32_t *smax) {
     const int g = lane >> 2, t = lane & 3;
     const int tok = 8 * o + g;
     const bool live = tok < ntok;
     const float *xc = x + (int64_t)tok * nb * 256 + (int64_t)j * 256 + 4 * t;
-    float4 v[16];
+    float4 v[4];
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-        v[k] = live ? __ldg(reinterpret_cast<const float4 *>(xc + 16 * k))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int kk = 0; kk < 4; ++kk)
+        v[kk] = live ? __ldg(reinterpret_cast<const float4 *>(xc + 16 * (4 * q + kk)))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     uint32_t m = 0;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        m = max(m, __float_as_uint(v[k].x) & 0x7FFFFFFFu);
-        m = max(m, __float_as_uint(v[k].y) & 0x7FFFFFFFu);
-        m = max(m, __float_as_uint(v[k].z) & 0x7FFFFFFFu);
-        m = max(m, __float_as_uint(v[k].w) & 0x7FFFFFFFu);
+    for (int kk = 0; kk < 4; ++kk) {
+        m = max(m, __float_as_uint(v[kk].x) & 0x7FFFFFFFu);
+        m = max(m, __float_as_uint(v[kk].y) & 0x7FFFFFFFu);
+        m = max(m, __float_as_uint(v[kk].z) & 0x7FFFFFFFu);
+        m = max(m, __float_as_uint(v[kk].w) & 0x7FFFFFFFu);
     }
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    if (t == 0) smax[q * 8 + g] = m;
+    __syncthreads();
+#pragma unroll
+    for (int qq = 0; qq < kTcPrepSplit; ++qq) m = max(m, smax[qq * 8 + g]);
     const bool finite = m < 0x7F800000u;
     // m < 2^E for E = (biased exponent of m) - 126; zero and subnormal
     // maxima take the exponent of the smallest normal
@@ -104,7 +112,7 @@ __device__ __forceinline__ void build_tc_record(const float *x, int ntok, int nb
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
         const int k = 4 * q + kk;
-        const float4 vk = q == 0 ? v[kk] : q == 1 ? v[4 + kk] : q == 2 ? v[8 + kk] : v[12 + kk];
+        const float4 vk = v[kk];
         const float xs[4] = {vk.x * s, vk.y * s, vk.z * s, vk.w * s};
         __half hi[4], lo[4];
         float part = 0.0f;

@@ -171,7 +171,7 @@ def test_noalloc_validates_before_any_cuda_call():
     assert lib.kq_matvec_noalloc(14, ctypes.c_void_p(1 << 30), 2, 256 * 125,
                                  ctypes.c_void_p(1 << 34), ctypes.c_void_p(1 << 36), 8,
                                  None) == 10  # KQ_ERR_LIMIT
-    assert lib.kq_status_str(10).decode().startswith("inputs exceed")
+    assert lib.kq_status_str(10).decode().startswith("a fixed buffer is too small")
 
 
 def test_dequant_rows_validates_before_any_cuda_call():

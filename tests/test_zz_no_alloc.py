@@ -115,4 +115,4 @@ def test_noalloc_rejects_records_beyond_its_buffer():
                  ntok) == KQ_ERR_LIMIT
     torch.cuda.synchronize()
     assert torch.all(y == 3.0), "a rejected call wrote its output"
-    assert lib.kq_status_str(KQ_ERR_LIMIT).decode().startswith("inputs exceed")
+    assert lib.kq_status_str(KQ_ERR_LIMIT).decode().startswith("a fixed buffer is too small")
