@@ -651,7 +651,7 @@ int64_t tc_records_bytes(const kq_mat *mats, int n, int ntok) {
 }
 
 cudaError_t prepare_tc_records(const kq_mat *mats, int n, int ntok, cudaStream_t s, uint8_t *buf,
-                               uint8_t **owned, const uint8_t **rec) {
+                               uint8_t **owned, const uint8_t **rec, bool overlap) {
     *owned = nullptr;
     const int64_t total = tc_records_bytes(mats, n, ntok);
     if (!buf) {
@@ -684,15 +684,15 @@ cudaError_t prepare_tc_records(const kq_mat *mats, int n, int ntok, cudaStream_t
     }
     p.first_warp[p.n] = warps;
     const int64_t blocks = (warps * 32 + kq::kTcPrepThreads - 1) / kq::kTcPrepThreads;
-    // With launch overlap on, the pass is scheduled while the kernel before
-    // it still runs and waits for it on the GPU (it writes nothing before
-    // that wait), so the launch latency is hidden.
+    // With `overlap`, the pass is scheduled while the kernel before it
+    // still runs and waits for it on the GPU (it writes nothing before that
+    // wait), so the launch latency is hidden.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kq::kTcPrepThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    if (g_overlap.load()) {
+    if (overlap) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -943,15 +943,25 @@ kq_status run_tc(const kq_mat *mats, int n, int ntok, cudaStream_t s) {
     // the streaming kernel, when forced but unable to take the call, fails
     // before anything is enqueued
     const int choice = kernel_choice();
-    if (choice == 2) {
-        kqplan::Plan PS;
+    bool streamed = false;
+    kqplan::Plan PS;
+    if (choice != 1) {
         const kq_status ps =
             kqplan::plan_stream(mats, n, ntok, info.sms, info.smem_optin, &PS, (ntok + 7) / 8);
-        if (ps != KQ_OK) return ps;
+        if (choice == 2 && ps != KQ_OK) return ps;
+        streamed = ps == KQ_OK && (choice == 2 || kqplan::tc_stream_preferred(PS));
     }
+    // With launch overlap on, the fragment pass overlaps the kernel before
+    // it -- except before a streaming launch whose CTAs cycle their ring
+    // (more stages than slots): there the early start of this call's CTAs
+    // competed with the previous call's last ones (the QKV set at 4-16
+    // columns, FFN gate/up and down and draft fc at 8: 2-5% slower), while
+    // launches whose whole weight share is in flight at once gained (Q4_K
+    // 4096x6656 at ntok 8: 12.96 -> 11.82 us per call).
+    const bool overlap = g_overlap.load() && (!streamed || PS.stages <= PS.nslot);
     const uint8_t *rec[KQ_MAX_SET];
     uint8_t *owned = nullptr;
-    e = prepare_tc_records(mats, n, ntok, s, nullptr, &owned, rec);
+    e = prepare_tc_records(mats, n, ntok, s, nullptr, &owned, rec, overlap);
     if (e != cudaSuccess) {
         g_last_cuda_error = (int)e;
         return KQ_ERR_CUDA;
@@ -1107,7 +1117,8 @@ kq_status run_noalloc(const kq_mat &in, int ntok, void *stream) {
         const uint8_t *rec[1];
         uint8_t *owned = nullptr;
         if (ce == cudaSuccess)
-            ce = prepare_tc_records(&m, 1, ntok, (cudaStream_t)stream, buf, &owned, rec);
+            ce = prepare_tc_records(&m, 1, ntok, (cudaStream_t)stream, buf, &owned, rec,
+                                    g_overlap.load());
         if (ce != cudaSuccess) {
             g_last_cuda_error = (int)ce;
             return KQ_ERR_CUDA;
