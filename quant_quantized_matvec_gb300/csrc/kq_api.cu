@@ -25,6 +25,10 @@ KQ_DECLARE_INSTANCES(5)
 KQ_DECLARE_INSTANCES(6)
 KQ_DECLARE_INSTANCES(7)
 KQ_DECLARE_INSTANCES(8)
+namespace kqlaunch {
+extern template cudaError_t launch_stream<1, true, false, kq::kStreamConsumersTall>(
+    const kq::StreamParams &, int, size_t, cudaStream_t);
+}
 
 namespace kqlaunch {
 cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s) {
@@ -40,9 +44,11 @@ cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cuda
     }
 }
 cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
-                   cudaStream_t s) {
+                   cudaStream_t s, bool tall) {
     switch (ntok * 2 + (xsmem ? 1 : 0)) {
-    case 3: return launch_stream<1, true>(p, grid, smem, s);
+    case 3:
+        return tall ? launch_stream<1, true, false, kq::kStreamConsumersTall>(p, grid, smem, s)
+                    : launch_stream<1, true>(p, grid, smem, s);
     case 2: return launch_stream<1, false>(p, grid, smem, s);
     case 5: return launch_stream<2, true>(p, grid, smem, s);
     case 4: return launch_stream<2, false>(p, grid, smem, s);
@@ -582,6 +588,10 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     const unsigned long long wl = g_wait_ns.load();
     p.wait_ns = wl ? wl : kq::kWaitLimitNs;
     const size_t smem = (size_t)P.smem;
+    // one token column, every member Q6_K, records in shared memory and 8
+    // or more stages a CTA (the Q6_K LM head, FFN down): 15 consumer warps
+    bool tall = ntok == 1 && xsmem && P.stages >= 8;
+    for (int i = 0; i < n; ++i) tall = tall && mats[i].fmt == KQ_Q6_K;
     *launched = true;
     GlobalRecords gr;
     cudaError_t e = cudaSuccess;
@@ -590,7 +600,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         for (int i = 0; i < n; ++i) p.m[i].rec = gr.rec[i];
     }
     if (e == cudaSuccess) {
-        e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s);
+        e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s, tall);
         if (gr.owned) {
             const cudaError_t ef = cudaFreeAsync(gr.buf, s);
             if (e == cudaSuccess) e = ef;

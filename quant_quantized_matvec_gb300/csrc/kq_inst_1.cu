@@ -2,3 +2,8 @@
 #include "kq_launch.cuh"
 
 KQ_DEFINE_INSTANCES(1)
+
+namespace kqlaunch {
+template cudaError_t launch_stream<1, true, false, kq::kStreamConsumersTall>(
+    const kq::StreamParams &, int, size_t, cudaStream_t);
+}

@@ -12,9 +12,10 @@
 //     (cp.async.bulk) per row segment, segments M.seg bytes apart, the
 //     sub-16-byte tail at the end of the matrix copied by the producer with
 //     plain loads.
-// Meanwhile the consumer warps turn the inputs into the fixed-point records
-// of kq_xrec.cuh in shared memory (or read them from global memory, where a
-// separate pass wrote them, when they do not fit).  Every consumer warp
+// The consumer warps, 12 (15 in the launch for tall Q6_K sets, NCW), turn
+// the inputs into the fixed-point records of kq_xrec.cuh in shared memory
+// (or read them from global memory, where a separate pass wrote them, when
+// they do not fit).  Every consumer warp
 // takes part in every stage: the stage's tasks -- one block column of two
 // rows, p and p + hp, that share their inputs -- ordered block-major so
 // neighbouring lanes share inputs, are dealt out 32 at a time round-robin
@@ -40,7 +41,13 @@
 namespace kq {
 
 constexpr int kStreamConsumers = 12;
-constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
+// Consumer warps of the one-token-column launch for Q6_K-only sets whose
+// CTAs stream many stages (kq_api.cu, run_stream): 16 warps, 128
+// registers each.  The Q6_K LM head 202048x6656 took 207.1 us per call
+// with them against 216.1, FFN down Q6_K 6656x19968 36.3 against 37.3;
+// other launches with 15 were slower (the QKV set 9.10 vs 8.85 us, the
+// Q5_K LM head 164.9 vs 156.5).
+constexpr int kStreamConsumersTall = 15;
 constexpr int kMaxMaps = 4;
 constexpr int kMaxSlots = 32;
 constexpr int kOverlapPrefetch = 1;  // stages issued before the inputs (overlap)
@@ -159,8 +166,9 @@ __device__ __forceinline__ void allow_dependents() {
 __device__ __forceinline__ void wait_prerequisites() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+template <int NCW>
 __device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"r"(kStreamConsumers * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
 }
 
 // Words of a Q6_K block staged in shared memory, 2-byte aligned: five
@@ -269,9 +277,10 @@ struct ConsumerCtx {
 // finish them, while the others go on): output (token tt, row r) is its nb
 // block partials added in block order, as for every group.  `nt` = token
 // columns of the partial buffer, `ntok` = token columns to store.
+template <int NCW>
 __device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, int ntok,
                                                   int warp, int lane) {
-    consumer_sync();
+    consumer_sync<NCW>();
     const int gl = c.G.ng - 1;
     const int64_t g0 = c.G.start(gl);
     const int h = (int)(c.G.start(gl + 1) - g0);
@@ -279,7 +288,7 @@ __device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, 
     const bool bad = *(volatile int *)c.abort_flag;
     const int nb = c.nb;
 #pragma unroll 1
-    for (int o = warp * 32 + lane; o < h * ntok; o += kStreamConsumers * 32) {
+    for (int o = warp * 32 + lane; o < h * ntok; o += NCW * 32) {
         const int tt = o / h, r = o - tt * h;
         const float *pp = pbuf + (int64_t)r * part_row_floats(nb, nt) + tt;
         float acc = pp[0];
@@ -289,7 +298,7 @@ __device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, 
     }
 }
 
-template <int NTOK, bool XSMEM, int FMT>
+template <int NTOK, bool XSMEM, int FMT, int NCW>
 __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane) {
     constexpr bool Q6 = FMT == kFmtQ6K;
     constexpr bool Q5 = FMT == kFmtQ5K;
@@ -301,16 +310,16 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
     const int tstride = nb * REC;
     const int prow = part_row_floats(nb, NTOK);
     if (XSMEM) {
-        build_records<Q6>(c.x, (int64_t)nb * 256, NTOK, nb, c.recs_w, warp, kStreamConsumers,
+        build_records<Q6>(c.x, (int64_t)nb * 256, NTOK, nb, c.recs_w, warp, NCW,
                           lane, [&] {
                               if (lane == 0)
                                   asm volatile("red.relaxed.cta.shared::cta.add.u32 [%0], 1;" ::"r"(
                                       smem_addr(c.xissued)));
                           });
-        consumer_sync();
+        consumer_sync<NCW>();
     }
     int batch_base = 0;
-    int rot = 0;  // batch_base % kStreamConsumers
+    int rot = 0;  // batch_base % NCW
     int slot = 0, lap = 0, g = 0, k = 0;
     int64_t g0 = c.G.start(0), g1 = c.G.start(1);
     int h = (int)(g1 - g0);
@@ -344,10 +353,10 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         if (ok) {
             // this warp's first batch: the one dealt to it in the rotation
             int dw = warp - rot;
-            if (dw < 0) dw += kStreamConsumers;
+            if (dw < 0) dw += NCW;
             int bat = batch_base + dw;
 #pragma unroll 1
-            for (; bat < batch_base + nbat; bat += kStreamConsumers) {
+            for (; bat < batch_base + nbat; bat += NCW) {
                 // Lanes past the stage's last task redo the last task and do
                 // not store it: the whole warp runs the block code together,
                 // which keeps its loops warp-uniform.
@@ -392,7 +401,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
         }
         batch_base += nbat;
         rot += nbat;
-        while (rot >= kStreamConsumers) rot -= kStreamConsumers;
+        while (rot >= NCW) rot -= NCW;
         __syncwarp();
         if (lane == 0) mbar_arrive(c.bars + 8 * (kMaxSlots + slot));
 
@@ -404,7 +413,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
                 old = atomicAdd(&c.gcount[g & 1], 1);
             }
             old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old == kStreamConsumers - 1) {
+            if (old == NCW - 1) {
                 __threadfence_block();
                 const bool bad = *(volatile int *)c.abort_flag;
                 if (lane < h) {
@@ -439,7 +448,7 @@ __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane
             hinv = c.hinv[hp];
         }
     }
-    reduce_last_group(c, NTOK, NTOK, warp, lane);
+    reduce_last_group<NCW>(c, NTOK, NTOK, warp, lane);
 }
 
 // One unit of a tensor-core launch: block column j of the stage (column
@@ -590,13 +599,14 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
             h = (int)(g1 - g0);
         }
     }
-    reduce_last_group(c, NT, c.ntok, warp, lane);
+    reduce_last_group<kStreamConsumers>(c, NT, c.ntok, warp, lane);
 }
 
-template <int NTOK, bool XSMEM, bool TC>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+template <int NTOK, bool XSMEM, bool TC, int NCW = kStreamConsumers>
+__global__ void __launch_bounds__(32 * (NCW + 1), 1)
     kq_set_stream(const __grid_constant__ StreamParams p) {
     static_assert(!TC || (NTOK % 8 == 0 && !XSMEM), "tensor-core launches: octets, global records");
+    static_assert(!TC || NCW == kStreamConsumers, "tensor-core launches: the scratch is sized for 12 warps");
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int abort_flag;
     __shared__ int gcount[2];  // warps done with the row group of each buffer
@@ -632,7 +642,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         abort_flag = 0;
         for (int s = 0; s < nslot; ++s) {
             mbar_init(bars + 8 * s, 1);
-            mbar_init(bars + 8 * (kMaxSlots + s), kStreamConsumers);
+            mbar_init(bars + 8 * (kMaxSlots + s), NCW);
         }
         mbar_init(xbar, 1);
         mbar_init(xbar + 8, 1);
@@ -642,7 +652,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
     __syncthreads();
 
-    if (warp == kStreamConsumers) {
+    if (warp == NCW) {
         // ------------------------------------------------ producer
         // Lane 0 takes every decision and every wait and shares the outcome
         // with the warp; the other lanes only help issue Q6_K row-segment
@@ -658,7 +668,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         auto wait_inputs_issued = [&]() {
             if (lane == 0) {
                 const unsigned long long t0 = global_ns();
-                while (*(volatile int *)&xissued < kStreamConsumers) {
+                while (*(volatile int *)&xissued < NCW) {
                     __nanosleep(20);
                     if (global_ns() - t0 > p.wait_ns) {
                         atomicExch(&abort_flag, 1);
@@ -795,7 +805,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.part_f = reinterpret_cast<float *>(smem + (parts - bars));
     c.part_step = p.part_bufs == 2 ? p.part_bytes / 8 : 0;
     c.scr = reinterpret_cast<float *>(smem + (scrs - bars));
-    c.scr_tiles = p.scr_bytes >= kStreamConsumers * 2 * kTcScrBytes ? 2 : 1;
+    c.scr_tiles = p.scr_bytes >= NCW * 2 * kTcScrBytes ? 2 : 1;
     c.ntok = p.ntok;
     c.bars = bars;
     c.ring = ring;
@@ -826,11 +836,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             consume_tc<NTOK / 8, kFmtQ6K>(c, warp, lane);
     } else {
         if (fmt == kFmtQ4K)
-            consume<NTOK, XSMEM, kFmtQ4K>(c, warp, lane);
+            consume<NTOK, XSMEM, kFmtQ4K, NCW>(c, warp, lane);
         else if (fmt == kFmtQ5K)
-            consume<NTOK, XSMEM, kFmtQ5K>(c, warp, lane);
+            consume<NTOK, XSMEM, kFmtQ5K, NCW>(c, warp, lane);
         else
-            consume<NTOK, XSMEM, kFmtQ6K>(c, warp, lane);
+            consume<NTOK, XSMEM, kFmtQ6K, NCW>(c, warp, lane);
     }
 }
 

@@ -38,7 +38,7 @@ cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
     return cudaGetLastError();
 }
 
-template <int NTOK, bool XSMEM, bool TC = false>
+template <int NTOK, bool XSMEM, bool TC = false, int NCW = kq::kStreamConsumers>
 cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cudaStream_t s) {
     static std::mutex mu;
     static size_t configured[64] = {};
@@ -49,7 +49,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
     {
         std::lock_guard<std::mutex> lock(mu);
         if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM, TC>,
+            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM, TC, NCW>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             configured[dev] = smem;
@@ -57,7 +57,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kq::kStreamThreads);
+    cfg.blockDim = dim3(32 * (NCW + 1));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -67,7 +67,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM, TC>, p);
+    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM, TC, NCW>, p);
 }
 
 // Row gather + dequantization (kq_rows.cu).
@@ -76,8 +76,10 @@ cudaError_t rows(int fmt, const uint8_t *W, int64_t rows, int nb, const int32_t 
 
 // ntok-dispatching entry points (defined in kq_api.cu from the instances)
 cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
+// (tall: a one-column launch of Q6_K members whose CTAs stream many
+// stages, run with kq::kStreamConsumersTall consumer warps)
 cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
-                   cudaStream_t s);
+                   cudaStream_t s, bool tall);
 // tensor-core launches of noct octets of tokens (kq_inst_tc.cu)
 cudaError_t direct_tc(int noct, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t stream_tc(int noct, const kq::StreamParams &p, int grid, size_t smem,
