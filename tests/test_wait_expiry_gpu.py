@@ -88,3 +88,32 @@ def test_default_limit_is_restored_and_reported_clear():
     torch.cuda.synchronize()
     C.check(fmt, W, rows, cols, x, y.cpu().numpy(), what="default limit")
     assert not kq.device_error()
+
+
+@pytest.mark.parametrize("limit_ns", [1, 200])
+def test_expired_waits_in_the_launch_for_tall_q6k_sets(limit_ns):
+    """The same report from the one-column launch that a Q6_K-only set
+    whose CTAs stream 8 or more stages gets (15 consumer warps)."""
+    import ctypes
+    lib = _binding.load()
+    fmt, rows, cols, ntok = kq.Q6_K, 15200, 2560, 1
+    arr = (_binding.KqMat * 1)()
+    arr[0].fmt, arr[0].rows, arr[0].cols = fmt, rows, cols
+    arr[0].W = arr[0].x = arr[0].y = 16 << 20  # never read
+    out = (ctypes.c_int64 * 64)()
+    props = torch.cuda.get_device_properties(0)
+    smem = getattr(props, "shared_memory_per_block_optin", 232448)  # GB300: 227 KB
+    assert lib.kq_plan_describe(arr, 1, ntok, props.multi_processor_count, smem, out, 64) == 0
+    assert out[0] == 0 and out[3] == 1 and out[9] >= 8  # planned, records in smem, 8+ stages
+    assert not kq.device_error(clear=True)
+    W, x = C.case(fmt, rows, cols, ntok, "expiry/tall")
+    g = C.Guarded(ntok, rows)
+    members = [(fmt, C.to_dev(W), rows, cols, C.to_dev(x), g.y)]
+    _expiring_call(lib, members, ntok, limit_ns)
+    assert kq.device_error(clear=True), "no expired wait was reported"
+    assert _nan_or_correct(fmt, W, rows, cols, x, g.host()) > 0
+    g.y.fill_(float("nan"))
+    kq.matvec_set(members, ntok=ntok)
+    torch.cuda.synchronize()
+    C.check(fmt, W, rows, cols, x, g.host(), what="tall Q6_K set after an expired call")
+    assert not kq.device_error()
