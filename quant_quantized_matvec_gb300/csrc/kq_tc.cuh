@@ -245,6 +245,15 @@ __device__ __forceinline__ void tc_unit_mt(RowP rowp, int nvalid, const uint8_t 
                     wa[m][hf] = tc_ld<GW, uint32_t>(pa[m] + QS + 32 * gp + 16 * hf + 4 * t);
                     wb[m][hf] = tc_ld<GW, uint32_t>(pb[m] + QS + 32 * gp + 16 * hf + 4 * t);
                 }
+            // one octet: the two sub-blocks' scales of row g in one 8-byte
+            // load (row g + 8's too spilled registers and slowed the Q6_K
+            // path of the same kernel; at two octets, scalar loads)
+            float2 fa2[MT];
+            if constexpr (NOCT == 1) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    fa2[m] = *reinterpret_cast<const float2 *>(Fa[m] + 2 * gp);
+            }
 #pragma unroll
             for (int hi = 0; hi < 2; ++hi) {
                 const int s = 2 * gp + hi;
@@ -262,8 +271,13 @@ __device__ __forceinline__ void tc_unit_mt(RowP rowp, int nvalid, const uint8_t 
                         }
                         tc_a_from_bytes(ca, cb, Q5 ? m5 : m4, A[m][hf]);
                     }
-                    fa[m] = Fa[m][s];
-                    fb[m] = Fb[m][s];
+                    if constexpr (NOCT == 1) {
+                        fa[m] = hi ? fa2[m].y : fa2[m].x;
+                        fb[m] = Fb[m][s];
+                    } else {
+                        fa[m] = Fa[m][s];
+                        fb[m] = Fb[m][s];
+                    }
                 }
 #pragma unroll
                 for (int o = 0; o < NOCT; ++o) {
@@ -306,7 +320,18 @@ __device__ __forceinline__ void tc_unit_mt(RowP rowp, int nvalid, const uint8_t 
                 for (int m = 0; m < MT; ++m)
 #pragma unroll
                     for (int k2 = 0; k2 < 2; ++k2) {
-                        const float *dm = (k2 ? Fb[m] : Fa[m]) + 16;
+                        // dm_0..dm_7 of the row (one octet: 16-byte loads)
+                        const float *dp = (k2 ? Fb[m] : Fa[m]) + 16;
+                        float dm[8];
+                        if constexpr (NOCT == 1) {
+                            const float4 d0 = *reinterpret_cast<const float4 *>(dp);
+                            const float4 d1 = *reinterpret_cast<const float4 *>(dp + 4);
+                            dm[0] = d0.x; dm[1] = d0.y; dm[2] = d0.z; dm[3] = d0.w;
+                            dm[4] = d1.x; dm[5] = d1.y; dm[6] = d1.z; dm[7] = d1.w;
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) dm[q] = dp[q];
+                        }
                         float mt = dm[0] * S[0];
 #pragma unroll
                         for (int s = 1; s < 8; ++s) mt = fmaf(dm[s], S[s], mt);
