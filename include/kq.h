@@ -212,11 +212,14 @@ int64_t kq_workspace_bytes(const kq_mat *mats, int n, int ntok);
 /*
  * kq_matvec_set with a caller-provided device workspace instead of the
  * library's stream-ordered temporaries: the call allocates nothing, so the
- * work it enqueues is kernels only.  In a CUDA graph, or a stream with
- * launch overlap on (kq_set_overlap), each call's input pass (the tensor-
- * core fragments, the staging of host inputs) then overlaps the kernel
- * before it, where an allocation between the kernels would have made it
- * wait for that kernel to finish and launch afterwards.
+ * work it enqueues is kernels only.  With launch overlap on
+ * (kq_set_overlap), in a CUDA graph or a stream, the tensor-core fragment
+ * pass can then start while the kernel before it still runs, where an
+ * allocation between the kernels would have made it wait for that kernel
+ * to finish and launch afterwards.  The library launches it that way
+ * before a direct-load launch and before a streaming launch whose CTAs
+ * keep all their weight stages in flight at once, where it was measured
+ * faster.
  *
  *   ws        device (or managed) memory of the current device, 256-byte
  *             aligned, not overlapping any member's W, x or y.  Owned by the
