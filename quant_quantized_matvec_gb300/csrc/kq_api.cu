@@ -101,7 +101,12 @@ struct StageParams {
 constexpr int kStageThreads = 256;
 
 __global__ void __launch_bounds__(kStageThreads) kq_xstage(const __grid_constant__ StageParams p) {
+    // the matvec after this copy may start at once (it streams its weights
+    // and waits for the copy before reading x); with launch overlap on this
+    // copy itself is launched while the kernel before it still runs, and
+    // waits for it before reading x or writing anything (a no-op otherwise)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t i = (int64_t)blockIdx.x * kStageThreads + threadIdx.x;
     if (i >= p.first[p.n]) return;
     int k = 0;
@@ -929,7 +934,19 @@ cudaError_t stage_inputs(kq_mat *mats, int n, int ntok, const bool *x_host, cuda
     for (int k = 0; k < p.n; ++k)
         p.dst[k] = reinterpret_cast<float4 *>(static_cast<uint8_t *>(*buf) + off[k]);
     const int64_t blocks = (p.first[p.n] + kq::kStageThreads - 1) / kq::kStageThreads;
-    kq::kq_xstage<<<(unsigned)blocks, kq::kStageThreads, 0, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kq::kStageThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (g_overlap.load()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kq::kq_xstage, p);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     for (int i = 0; i < n; ++i)
