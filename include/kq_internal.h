@@ -15,7 +15,7 @@ extern "C" {
 
 /* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
  * KQ_PLAN_MEMBER per member. */
-#define KQ_PLAN_HEAD 13
+#define KQ_PLAN_HEAD 14
 #define KQ_PLAN_MEMBER 21
 
 /*
@@ -38,7 +38,10 @@ extern "C" {
  *   the streaming kernel for this plan under automatic kernel selection,
  *   0 if it takes the direct-load kernel (two octets of tokens and several
  *   row groups a CTA that fill less than four fifths of their 16-row
- *   tiles); 0 for dp4a launches and failed plans
+ *   tiles); 0 for dp4a launches and failed plans  [13] consumer warps of the
+ *   streaming launch (12; 15 for one token column of Q6_K-only members
+ *   with records in shared memory and 8 or more stages a CTA); 0 for
+ *   failed plans
  *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
  *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes, whole (Q6_K
  *   stages of whole rows, one bulk copy each: 1; else 0).

@@ -593,10 +593,8 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     const unsigned long long wl = g_wait_ns.load();
     p.wait_ns = wl ? wl : kq::kWaitLimitNs;
     const size_t smem = (size_t)P.smem;
-    // one token column, every member Q6_K, records in shared memory and 8
-    // or more stages a CTA (the Q6_K LM head, FFN down): 15 consumer warps
-    bool tall = ntok == 1 && xsmem && P.stages >= 8;
-    for (int i = 0; i < n; ++i) tall = tall && mats[i].fmt == KQ_Q6_K;
+    // 15 consumer warps for tall Q6_K sets at one token column
+    const bool tall = kqplan::stream_consumers(P, mats, n) == kq::kStreamConsumersTall;
     *launched = true;
     GlobalRecords gr;
     cudaError_t e = cudaSuccess;

@@ -267,6 +267,12 @@ bool tc_stream_preferred(const Plan &P) {
     return true;
 }
 
+int stream_consumers(const Plan &P, const kq_mat *mats, int n) {
+    bool tall = P.tc_noct == 0 && P.ntok == 1 && P.xsmem && P.stages >= 8;
+    for (int i = 0; i < n; ++i) tall = tall && mats[i].fmt == KQ_Q6_K;
+    return tall ? kq::kStreamConsumersTall : kq::kStreamConsumers;
+}
+
 }  // namespace kqplan
 
 extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
@@ -292,6 +298,7 @@ extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, in
     *o++ = P.scr_bytes;
     *o++ = P.part_bufs;
     *o++ = st == KQ_OK && noct > 0 ? (kqplan::tc_stream_preferred(P) ? 1 : 0) : 0;
+    *o++ = st == KQ_OK ? kqplan::stream_consumers(P, mats, n) : 0;
     for (int i = 0; i < n; ++i) {
         const kqplan::Member &M = P.m[i];
         const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],

@@ -65,6 +65,12 @@ constexpr int64_t kCostQ6 = 32;
 // rows) ran faster streamed.  One octet: always true.
 bool tc_stream_preferred(const Plan &P);
 
+// Consumer warps of a dp4a streaming launch: kq::kStreamConsumersTall (15)
+// for one token column of Q6_K-only members with records in shared memory
+// and 8 or more stages a CTA (the Q6_K LM head, FFN down), else
+// kq::kStreamConsumers (12).  Tensor-core launches: kq::kStreamConsumers.
+int stream_consumers(const Plan &P, const kq_mat *mats, int n);
+
 kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out,
                       int tc_noct = 0);
 

@@ -11,7 +11,7 @@ import pytest
 
 from quant_quantized_matvec_gb300 import _binding
 
-HEAD, MEMBER = 13, 21
+HEAD, MEMBER = 14, 21
 TC_MIN = 4                      # ntok from which the tensor-core path runs
 TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps, one 16-row tile
 # ... and two tiles where units span both tiles of a group (ntok 9..16, groups of 17+ rows)
@@ -32,7 +32,7 @@ def plan(members, ntok, sms=SMS, smem=SMEM):
     o = list(out)
     head = dict(zip(["status", "grid", "level", "xsmem", "x_bytes", "part_bytes",
                      "slot_bytes", "nslot", "smem", "stages", "scr_bytes", "part_bufs",
-                     "tc_stream"],
+                     "tc_stream", "ncw"],
                     o[:HEAD]))
     keys = ["ncta", "cta_begin", "rows_q", "rows_r", "ng0", "gq0", "gr0", "ng1", "gq1",
             "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes",
@@ -208,3 +208,22 @@ def test_shapes_the_stream_kernel_cannot_stage():
 def test_plan_is_deterministic():
     members = [(12, 4096, 6656), (14, 256, 6656), (13, 777, 2560)]
     assert plan(members, 3) == plan(members, 3)
+
+
+@pytest.mark.parametrize("members,ntok,ncw", [
+    ([(14, 202048, 6656)], 1, 15),                   # Q6_K LM head
+    ([(14, 4096, 17920)], 1, 15),                    # Q6_K FFN down
+    ([(14, 202048, 6656)], 2, 12),                   # two token columns
+    ([(12, 202048, 6656)], 1, 12),                   # Q4_K LM head
+    ([(12, 4096, 6656), (14, 256, 6656)], 1, 12),    # mixed set
+    ([(14, 256, 6656)], 1, 12),                      # one stage a CTA
+    ([(14, 202048, 6656)], 8, 12),                   # tensor-core launch
+])
+def test_consumer_warps(members, ntok, ncw):
+    """Consumer warps of the launch (kq_plan.h, stream_consumers): 15 only
+    for one token column of Q6_K-only sets with records in shared memory
+    and 8 or more stages a CTA, else 12; tensor-core launches always 12."""
+    h, _ = plan(members, ntok)
+    assert h["status"] == OK and h["ncw"] == ncw
+    if ncw == 15:
+        assert h["xsmem"] == 1 and h["stages"] >= 8
