@@ -81,6 +81,11 @@ def workload(name: str, ntok: int):
                 "grid-split pair Q6_K + Q5_K 2560->512, separate x planes")
     if name == "lm_head_q6k":
         return ([(Q6_K, 202048, 6656, 0)], "LM head Q6_K 202048x6656")
+    if name == "lm_head_q6k_slice":
+        # the LM head's launch form (whole-row stages, 15 consumer warps) on
+        # 260 rows a CTA: 216 MB, above L2, small enough for a many-pass ncu
+        # capture
+        return ([(Q6_K, 39520, 6656, 0)], "LM head Q6_K rows 0..39519 (39520x6656)")
     # further release shapes ("Chapter 6 - The kquant family on the
     # reference lane", Figure 6.6; n_in -> n_out is cols -> rows)
     if name == "ffn_gate_up_set":
