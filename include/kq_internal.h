@@ -15,7 +15,7 @@ extern "C" {
 
 /* Entries of kq_plan_describe's output: KQ_PLAN_HEAD for the launch, then
  * KQ_PLAN_MEMBER per member. */
-#define KQ_PLAN_HEAD 14
+#define KQ_PLAN_HEAD 15
 #define KQ_PLAN_MEMBER 21
 
 /*
@@ -41,6 +41,8 @@ extern "C" {
  *   tiles); 0 for dp4a launches and failed plans  [13] consumer warps of the
  *   streaming launch (12; 15 for one token column of Q6_K-only members
  *   with records in shared memory and 8 or more stages a CTA); 0 for
+ *   failed plans  [14] rows of one lane-task in a dp4a launch (2; 1 in
+ *   the 15-warp launch when no member is staged in whole rows); 0 for
  *   failed plans
  *   then per member: ncta, cta_begin, rows_q, rows_r, ng0, gq0, gr0, ng1,
  *   gq1, gr1, rmax, kb, seg, hmax, nh, hs0..hs3, row_bytes, whole (Q6_K

@@ -28,6 +28,8 @@ KQ_DECLARE_INSTANCES(8)
 namespace kqlaunch {
 extern template cudaError_t launch_stream<1, true, false, kq::kStreamConsumersTall>(
     const kq::StreamParams &, int, size_t, cudaStream_t);
+extern template cudaError_t launch_stream<1, true, false, kq::kStreamConsumersTall, 1>(
+    const kq::StreamParams &, int, size_t, cudaStream_t);
 }
 
 namespace kqlaunch {
@@ -44,9 +46,11 @@ cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cuda
     }
 }
 cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
-                   cudaStream_t s, bool tall) {
+                   cudaStream_t s, bool tall, int rpt) {
     switch (ntok * 2 + (xsmem ? 1 : 0)) {
     case 3:
+        if (tall && rpt == 1)
+            return launch_stream<1, true, false, kq::kStreamConsumersTall, 1>(p, grid, smem, s);
         return tall ? launch_stream<1, true, false, kq::kStreamConsumersTall>(p, grid, smem, s)
                     : launch_stream<1, true>(p, grid, smem, s);
     case 2: return launch_stream<1, false>(p, grid, smem, s);
@@ -593,8 +597,10 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
     const unsigned long long wl = g_wait_ns.load();
     p.wait_ns = wl ? wl : kq::kWaitLimitNs;
     const size_t smem = (size_t)P.smem;
-    // 15 consumer warps for tall Q6_K sets at one token column
+    // 15 consumer warps for tall Q6_K sets at one token column, one row a
+    // lane-task when they are staged in row segments
     const bool tall = kqplan::stream_consumers(P, mats, n) == kq::kStreamConsumersTall;
+    const int rpt = kqplan::stream_rows_per_lane(P, mats, n);
     *launched = true;
     GlobalRecords gr;
     cudaError_t e = cudaSuccess;
@@ -603,7 +609,7 @@ kq_status run_stream(const kq_mat *mats, int n, int ntok, cudaStream_t s,
         for (int i = 0; i < n; ++i) p.m[i].rec = gr.rec[i];
     }
     if (e == cudaSuccess) {
-        e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s, tall);
+        e = kqlaunch::stream(ntok, xsmem, p, cta, smem, s, tall, rpt);
         if (gr.owned) {
             const cudaError_t ef = cudaFreeAsync(gr.buf, s);
             if (e == cudaSuccess) e = ef;

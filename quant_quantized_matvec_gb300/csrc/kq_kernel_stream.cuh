@@ -17,10 +17,12 @@
 // (or read them from global memory, where a separate pass wrote them, when
 // they do not fit).  Every consumer warp
 // takes part in every stage: the stage's tasks -- one block column of two
-// rows, p and p + hp, that share their inputs -- ordered block-major so
-// neighbouring lanes share inputs, are dealt out 32 at a time round-robin
-// over the consumer warps; each lane turns its two super-blocks into
-// per-token partial sums (kq_blocks.cuh) stored in shared memory.  When a
+// rows, p and p + hp, that share their inputs (of one row, RPT = 1, in the
+// launch for tall Q6_K sets staged in row segments) -- ordered block-major
+// so neighbouring lanes share inputs, are dealt out 32 at a time
+// round-robin over the consumer warps; each lane turns its super-blocks
+// into per-token partial sums (kq_blocks.cuh) stored in shared memory.  A
+// row's partial is the same whichever rows share its task.  When a
 // row group's last stage is done, the last warp to finish it sums each
 // row's blocks in block order 0..nb-1 and writes y; the CTA's last group is
 // summed the same way by all consumer warps together.  That sum order, and
@@ -240,7 +242,9 @@ __host__ __device__ __forceinline__ int part_row_floats(int nb, int nt) { return
 __device__ __forceinline__ int pair_offset(int h) { return (h + 1) >> 1; }
 
 // Rows of one task: a lane takes one block column of R rows of the stage,
-// p and p + hp, which share their inputs.
+// p and p + hp, which share their inputs.  R = 2, except in the launch for
+// tall Q6_K sets staged in row segments (kq_plan.h, stream_rows_per_lane),
+// which takes R = 1: the template parameter RPT of kq_set_stream.
 __host__ __device__ constexpr int stream_rows_per_task(int fmt, int ntok) {
     return (void)fmt, (void)ntok, 2;
 }
@@ -298,13 +302,14 @@ __device__ __forceinline__ void reduce_last_group(const ConsumerCtx &c, int nt, 
     }
 }
 
-template <int NTOK, bool XSMEM, int FMT, int NCW>
+template <int NTOK, bool XSMEM, int FMT, int NCW, int RPT>
 __device__ __forceinline__ void consume(const ConsumerCtx &c, int warp, int lane) {
     constexpr bool Q6 = FMT == kFmtQ6K;
     constexpr bool Q5 = FMT == kFmtQ5K;
     constexpr int BB = Q6 ? 210 : (Q5 ? 176 : 144);
     constexpr int REC = rec_bytes(Q6);
-    constexpr int R = stream_rows_per_task(FMT, NTOK);
+    constexpr int R = RPT;
+    static_assert(R == 1 || R == 2, "one or two rows a task");
     using XR = Rec<!XSMEM>;
     const int nb = c.nb;
     const int tstride = nb * REC;
@@ -602,7 +607,7 @@ __device__ __forceinline__ void consume_tc(const ConsumerCtx &c, int warp, int l
     reduce_last_group<kStreamConsumers>(c, NT, c.ntok, warp, lane);
 }
 
-template <int NTOK, bool XSMEM, bool TC, int NCW = kStreamConsumers>
+template <int NTOK, bool XSMEM, bool TC, int NCW = kStreamConsumers, int RPT = 2>
 __global__ void __launch_bounds__(32 * (NCW + 1), 1)
     kq_set_stream(const __grid_constant__ StreamParams p) {
     static_assert(!TC || (NTOK % 8 == 0 && !XSMEM), "tensor-core launches: octets, global records");
@@ -836,11 +841,11 @@ __global__ void __launch_bounds__(32 * (NCW + 1), 1)
             consume_tc<NTOK / 8, kFmtQ6K>(c, warp, lane);
     } else {
         if (fmt == kFmtQ4K)
-            consume<NTOK, XSMEM, kFmtQ4K, NCW>(c, warp, lane);
+            consume<NTOK, XSMEM, kFmtQ4K, NCW, RPT>(c, warp, lane);
         else if (fmt == kFmtQ5K)
-            consume<NTOK, XSMEM, kFmtQ5K, NCW>(c, warp, lane);
+            consume<NTOK, XSMEM, kFmtQ5K, NCW, RPT>(c, warp, lane);
         else
-            consume<NTOK, XSMEM, kFmtQ6K, NCW>(c, warp, lane);
+            consume<NTOK, XSMEM, kFmtQ6K, NCW, RPT>(c, warp, lane);
     }
 }
 

@@ -38,7 +38,7 @@ cudaError_t launch_direct(const kq::SetParams &p, int grid, size_t smem,
     return cudaGetLastError();
 }
 
-template <int NTOK, bool XSMEM, bool TC = false, int NCW = kq::kStreamConsumers>
+template <int NTOK, bool XSMEM, bool TC = false, int NCW = kq::kStreamConsumers, int RPT = 2>
 cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cudaStream_t s) {
     static std::mutex mu;
     static size_t configured[64] = {};
@@ -49,7 +49,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
     {
         std::lock_guard<std::mutex> lock(mu);
         if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM, TC, NCW>,
+            e = cudaFuncSetAttribute(kq::kq_set_stream<NTOK, XSMEM, TC, NCW, RPT>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             configured[dev] = smem;
@@ -67,7 +67,7 @@ cudaError_t launch_stream(const kq::StreamParams &p, int grid, size_t smem, cuda
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM, TC, NCW>, p);
+    return cudaLaunchKernelEx(&cfg, kq::kq_set_stream<NTOK, XSMEM, TC, NCW, RPT>, p);
 }
 
 // Row gather + dequantization (kq_rows.cu).
@@ -77,9 +77,10 @@ cudaError_t rows(int fmt, const uint8_t *W, int64_t rows, int nb, const int32_t 
 // ntok-dispatching entry points (defined in kq_api.cu from the instances)
 cudaError_t direct(int ntok, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
 // (tall: a one-column launch of Q6_K members whose CTAs stream many
-// stages, run with kq::kStreamConsumersTall consumer warps)
+// stages, run with kq::kStreamConsumersTall consumer warps; rpt: rows a
+// lane-task, 2, or 1 for tall sets staged in row segments)
 cudaError_t stream(int ntok, bool xsmem, const kq::StreamParams &p, int grid, size_t smem,
-                   cudaStream_t s, bool tall);
+                   cudaStream_t s, bool tall, int rpt);
 // tensor-core launches of noct octets of tokens (kq_inst_tc.cu)
 cudaError_t direct_tc(int noct, const kq::SetParams &p, int grid, size_t smem, cudaStream_t s);
 cudaError_t stream_tc(int noct, const kq::StreamParams &p, int grid, size_t smem,

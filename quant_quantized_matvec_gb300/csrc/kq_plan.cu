@@ -273,6 +273,13 @@ int stream_consumers(const Plan &P, const kq_mat *mats, int n) {
     return tall ? kq::kStreamConsumersTall : kq::kStreamConsumers;
 }
 
+int stream_rows_per_lane(const Plan &P, const kq_mat *mats, int n) {
+    if (stream_consumers(P, mats, n) != kq::kStreamConsumersTall) return 2;
+    for (int i = 0; i < n; ++i)
+        if (P.m[i].whole) return 2;
+    return 1;
+}
+
 }  // namespace kqplan
 
 extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, int smem_optin,
@@ -299,6 +306,7 @@ extern "C" int kq_plan_describe(const kq_mat *mats, int n, int ntok, int sms, in
     *o++ = P.part_bufs;
     *o++ = st == KQ_OK && noct > 0 ? (kqplan::tc_stream_preferred(P) ? 1 : 0) : 0;
     *o++ = st == KQ_OK ? kqplan::stream_consumers(P, mats, n) : 0;
+    *o++ = st == KQ_OK ? kqplan::stream_rows_per_lane(P, mats, n) : 0;
     for (int i = 0; i < n; ++i) {
         const kqplan::Member &M = P.m[i];
         const int64_t v[KQ_PLAN_MEMBER] = {M.ncta, M.cta_begin, M.rows_q, M.rows_r, M.ng[0],

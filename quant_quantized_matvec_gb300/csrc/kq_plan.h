@@ -71,6 +71,14 @@ bool tc_stream_preferred(const Plan &P);
 // kq::kStreamConsumers (12).  Tensor-core launches: kq::kStreamConsumers.
 int stream_consumers(const Plan &P, const kq_mat *mats, int n);
 
+// Rows of one lane-task in a dp4a streaming launch: 1 for the 15-warp
+// launch of tall Q6_K sets when no member is staged in whole rows (FFN
+// down: 34.4 against 36.4 us with 2; with whole-row stages, the LM head,
+// one row a task took 254 against 207 us), else 2.  Tensor-core launches:
+// 2 (unused).  A task count h x kb stays below 2^12 either way: segment
+// stages hold at most 32 rows of at most 9 Q6_K blocks.
+int stream_rows_per_lane(const Plan &P, const kq_mat *mats, int n);
+
 kq_status plan_stream(const kq_mat *mats, int n, int ntok, int sms, int smem_optin, Plan *out,
                       int tc_noct = 0);
 

@@ -11,7 +11,7 @@ import pytest
 
 from quant_quantized_matvec_gb300 import _binding
 
-HEAD, MEMBER = 14, 21
+HEAD, MEMBER = 15, 21
 TC_MIN = 4                      # ntok from which the tensor-core path runs
 TC_SCR = 12 * 16 * 28 * 4       # its unit scratch: 12 consumer warps, one 16-row tile
 # ... and two tiles where units span both tiles of a group (ntok 9..16, groups of 17+ rows)
@@ -32,7 +32,7 @@ def plan(members, ntok, sms=SMS, smem=SMEM):
     o = list(out)
     head = dict(zip(["status", "grid", "level", "xsmem", "x_bytes", "part_bytes",
                      "slot_bytes", "nslot", "smem", "stages", "scr_bytes", "part_bufs",
-                     "tc_stream", "ncw"],
+                     "tc_stream", "ncw", "rpt"],
                     o[:HEAD]))
     keys = ["ncta", "cta_begin", "rows_q", "rows_r", "ng0", "gq0", "gr0", "ng1", "gq1",
             "gr1", "rmax", "kb", "seg", "hmax", "nh", "hs0", "hs1", "hs2", "hs3", "row_bytes",
@@ -210,20 +210,30 @@ def test_plan_is_deterministic():
     assert plan(members, 3) == plan(members, 3)
 
 
-@pytest.mark.parametrize("members,ntok,ncw", [
-    ([(14, 202048, 6656)], 1, 15),                   # Q6_K LM head
-    ([(14, 4096, 17920)], 1, 15),                    # Q6_K FFN down
-    ([(14, 202048, 6656)], 2, 12),                   # two token columns
-    ([(12, 202048, 6656)], 1, 12),                   # Q4_K LM head
-    ([(12, 4096, 6656), (14, 256, 6656)], 1, 12),    # mixed set
-    ([(14, 256, 6656)], 1, 12),                      # one stage a CTA
-    ([(14, 202048, 6656)], 8, 12),                   # tensor-core launch
+@pytest.mark.parametrize("members,ntok,ncw,rpt", [
+    ([(14, 202048, 6656)], 1, 15, 2),                # Q6_K LM head (whole rows)
+    ([(14, 39520, 6656)], 1, 15, 2),                 # its 39520-row slice
+    ([(14, 6656, 19968)], 1, 15, 1),                 # Q6_K FFN down (segments)
+    ([(14, 4096, 17920)], 1, 15, 1),
+    ([(14, 15200, 2560)], 1, 15, 1),
+    ([(14, 202048, 6656)], 2, 12, 2),                # two token columns
+    ([(12, 202048, 6656)], 1, 12, 2),                # Q4_K LM head
+    ([(12, 4096, 6656), (14, 256, 6656)], 1, 12, 2),  # mixed set
+    ([(14, 4096, 6656)], 1, 12, 2),                  # 3 stages a CTA
+    ([(14, 256, 6656)], 1, 12, 2),                   # one stage a CTA
+    ([(14, 202048, 6656)], 8, 12, 2),                # tensor-core launch
 ])
-def test_consumer_warps(members, ntok, ncw):
+def test_consumer_warps_and_task_rows(members, ntok, ncw, rpt):
     """Consumer warps of the launch (kq_plan.h, stream_consumers): 15 only
     for one token column of Q6_K-only sets with records in shared memory
-    and 8 or more stages a CTA, else 12; tensor-core launches always 12."""
-    h, _ = plan(members, ntok)
-    assert h["status"] == OK and h["ncw"] == ncw
+    and 8 or more stages a CTA, else 12; tensor-core launches always 12.
+    Rows a lane-task (stream_rows_per_lane): 1 only in that 15-warp launch
+    when no member is staged in whole rows."""
+    h, mem = plan(members, ntok)
+    assert h["status"] == OK and h["ncw"] == ncw and h["rpt"] == rpt
     if ncw == 15:
         assert h["xsmem"] == 1 and h["stages"] >= 8
+        assert rpt == (1 if not any(m["whole"] for m in mem) else 2)
+    if rpt == 1:
+        # one row a task: a stage's tasks are h x kb, below 2^12
+        assert all(m["hmax"] * m["kb"] < 4096 for m in mem)

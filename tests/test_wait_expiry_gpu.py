@@ -90,13 +90,15 @@ def test_default_limit_is_restored_and_reported_clear():
     assert not kq.device_error()
 
 
+@pytest.mark.parametrize("rows,cols,rpt", [(15200, 2560, 1), (39520, 6656, 2)])
 @pytest.mark.parametrize("limit_ns", [1, 200])
-def test_expired_waits_in_the_launch_for_tall_q6k_sets(limit_ns):
+def test_expired_waits_in_the_launch_for_tall_q6k_sets(limit_ns, rows, cols, rpt):
     """The same report from the one-column launch that a Q6_K-only set
-    whose CTAs stream 8 or more stages gets (15 consumer warps)."""
+    whose CTAs stream 8 or more stages gets (15 consumer warps), with one
+    row a lane-task (row-segment stages) and with two (whole-row stages)."""
     import ctypes
     lib = _binding.load()
-    fmt, rows, cols, ntok = kq.Q6_K, 15200, 2560, 1
+    fmt, ntok = kq.Q6_K, 1
     arr = (_binding.KqMat * 1)()
     arr[0].fmt, arr[0].rows, arr[0].cols = fmt, rows, cols
     arr[0].W = arr[0].x = arr[0].y = 16 << 20  # never read
@@ -105,6 +107,7 @@ def test_expired_waits_in_the_launch_for_tall_q6k_sets(limit_ns):
     smem = getattr(props, "shared_memory_per_block_optin", 232448)  # GB300: 227 KB
     assert lib.kq_plan_describe(arr, 1, ntok, props.multi_processor_count, smem, out, 64) == 0
     assert out[0] == 0 and out[13] == 15  # planned, 15 consumer warps
+    assert out[14] == rpt                 # rows a lane-task
     assert not kq.device_error(clear=True)
     W, x = C.case(fmt, rows, cols, ntok, "expiry/tall")
     g = C.Guarded(ntok, rows)
