@@ -136,6 +136,16 @@ def check(members, ntok, sms=SMS, smem=SMEM):
                     q, r = m[f"gq{big}"], m[f"gr{big}"]
                     fills += [hh / (16 * -(-hh // 16)) for hh in ([q, q + 1] if r else [q])]
         assert h["tc_stream"] == int(all(f >= 0.8 for f in fills))
+    # consumer warps: 15 only for one column of Q6_K-only sets with records
+    # in shared memory and 8 or more stages a CTA; one row a lane-task only
+    # there, and only without whole-row stages
+    tall = (ntok == 1 and h["xsmem"] == 1 and h["stages"] >= 8
+            and all(fmt == 14 for fmt, _, _ in members))
+    assert h["ncw"] == (15 if tall else 12)
+    one_row = tall and not any(m["whole"] for m in mem)
+    assert h["rpt"] == (1 if one_row else 2)
+    if one_row:
+        assert all(m["hmax"] * m["kb"] < 4096 for m in mem)
     return h, mem
 
 
