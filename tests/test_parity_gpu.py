@@ -111,6 +111,29 @@ def test_stream_equals_direct(fmt, ntok, rows, cols):
     C.check(fmt, W, rows, cols, x, outs["stream"], what="stream kernel")
 
 
+@pytest.mark.parametrize("rows,cols,rpt", [(15200, 2560, 1), (6656, 19968, 1),
+                                           (39520, 6656, 2)])
+def test_tall_q6k_stream_equals_direct(rows, cols, rpt):
+    """The 15-warp launch of tall Q6_K sets at one token column, with one
+    row a lane-task (row-segment stages: a 15200x2560 matrix, FFN down) and
+    with two (whole-row stages: a 39520-row slice of the LM head), against
+    the direct-load kernel: bitwise equal, and every output within the
+    contract of the oracle."""
+    import ctypes
+    from quant_quantized_matvec_gb300 import _binding
+    fmt, ntok = kq.Q6_K, 1
+    lib = _binding.load()
+    arr = (_binding.KqMat * 1)()
+    arr[0].fmt, arr[0].rows, arr[0].cols = fmt, rows, cols
+    arr[0].W = arr[0].x = arr[0].y = 16 << 20  # never read
+    out = (ctypes.c_int64 * 64)()
+    props = torch.cuda.get_device_properties(0)
+    smem = getattr(props, "shared_memory_per_block_optin", 232448)  # GB300: 227 KB
+    assert lib.kq_plan_describe(arr, 1, ntok, props.multi_processor_count, smem, out, 64) == 0
+    assert out[0] == 0 and out[13] == 15 and out[14] == rpt
+    test_stream_equals_direct(fmt, ntok, rows, cols)
+
+
 @pytest.mark.gpu
 def test_overlap_chain_equals_serial():
     """With launch overlap on, each call streams its weights while the call
