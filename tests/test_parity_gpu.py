@@ -5,6 +5,8 @@ multiple of the rows a CTA takes, odd block counts per row that leave Q6_K
 rows 2-byte aligned); the full-size workloads are the ones the benchmark
 times: Q4_K 256x6656; Q4_K/Q5_K/Q6_K 4096x6656 at ntok 1, 2, 4, 8 (every
 output); the 202048x6656 Q6_K LM head at ntok 1 and 4 (sampled rows).
+The streaming kernel is also compared bitwise with the direct-load kernel,
+on small shapes and on the tall Q6_K shapes of its 15-warp launch.
 """
 import numpy as np
 import pytest
