@@ -247,3 +247,26 @@ def test_consumer_warps_and_task_rows(members, ntok, ncw, rpt):
     if rpt == 1:
         # one row a task: a stage's tasks are h x kb, below 2^12
         assert all(m["hmax"] * m["kb"] < 4096 for m in mem)
+
+
+@pytest.mark.parametrize("ntok", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("name", ["qkv_gate_set", "q4k_4096", "q5k_4096", "q6k_4096",
+                                  "q4k_256", "cat_q6k_q5k", "lm_head_q6k",
+                                  "lm_head_q6k_slice", "ffn_gate_up_set", "ffn_down_q4k",
+                                  "ffn_down_q6k", "attn_output_q4k", "lm_head_q5k",
+                                  "draft_kv_set", "draft_fc_q4k"])
+def test_bench_workloads_plan(name, ntok):
+    """Every matvec workload the benchmark times plans a valid streaming
+    launch on a GB300 (the checks of `check`) at ntok up to 8; at 16,
+    where partials for 16 token columns leave the ring no room on some
+    shapes (the QKV set, the LM heads, FFN gate+up), the plan reports
+    KQ_ERR_SHAPE and the direct-load kernel runs, as it does when
+    automatic selection prefers it."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    members, _ = bench.workload(name, ntok)
+    h, _ = check([(f, r, c) for f, r, c, _ in members], ntok)
+    assert h["status"] == OK or (ntok > 8 and h["status"] == SHAPE), (name, ntok)
+
